@@ -1,0 +1,205 @@
+// asp_internal.cuh - device primitives and workspace layout shared by the
+// kernels of libasp.so (sm_103a). Nothing here is part of the C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "asp.h"
+
+namespace asp {
+
+constexpr int kMaxSegments = 4096;     // batch * Hkv handled by one call
+constexpr int kMaxPages = 1 << 20;     // max_pages bound (int32 page-space arithmetic)
+constexpr int kMaxGroup = 8;           // query heads per KV head (padded mma width)
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a bounded on-chip wait gives up after 2 s
+
+// ----------------------------------------------------------------- workspace
+// [ header 256 B | counters int32[S] | scores f32[S*max_pages] | partials ]
+// header word 0 is the sticky device error mask.
+struct WsLayout {
+  size_t counters_off = 0;
+  size_t scores_off = 0;
+  size_t partials_off = 0;
+  size_t total = 0;
+  int decode_grid = 0;   // CTAs of the decode kernel
+  int slot_floats = 0;   // floats per partial slot: m[8], l[8], o[8][d]
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline WsLayout ws_layout(const asp_paged_kv& kv, int num_sms) {
+  WsLayout w;
+  const size_t S = size_t(kv.batch) * kv.num_kv_heads;
+  w.decode_grid = num_sms;
+  w.slot_floats = 2 * kMaxGroup + kMaxGroup * kv.head_dim;
+  w.counters_off = 256;
+  w.scores_off = align256(w.counters_off + S * sizeof(int32_t));
+  w.partials_off = align256(w.scores_off + S * size_t(kv.max_pages) * sizeof(float));
+  w.total = align256(w.partials_off +
+                     (S + size_t(w.decode_grid)) * size_t(w.slot_floats) * sizeof(float));
+  return w;
+}
+
+// ------------------------------------------------------------- device errors
+__device__ __forceinline__ void report(uint32_t* err, uint32_t bits) {
+  if (err) atomicOr(err, bits);
+}
+
+// ------------------------------------------------------------------- helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Valid tokens of request b: seq_lens clamped to [0, max_pages*P]; a clamp
+// raises ASP_DEVERR_SEQ_RANGE.
+__device__ __forceinline__ int clamp_seq_len(int T, int max_pages, int P, uint32_t* err) {
+  const long long cap = (long long)max_pages * P;
+  if (T < 0 || (long long)T > cap) {
+    report(err, ASP_DEVERR_SEQ_RANGE);
+    return T < 0 ? 0 : (int)cap;
+  }
+  return T;
+}
+
+// ------------------------------------------------------------------ mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Waits until the phase with the given parity has completed. Returns false
+// (and the caller reports ASP_DEVERR_TIMEOUT) if that takes longer than
+// kWaitLimitNs: no wait in this library can spin forever.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// ----------------------------------------------------------- bulk / TMA copy
+// 1-D bulk copy global -> shared, completing `bytes` on the mbarrier.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// 2-D tiled TMA load of one box at (x, y). x is the innermost coordinate in
+// elements and must be a multiple of 8 for bf16 (16-byte rule).
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA) accesses to the same buffer.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Named barrier over a subset of the CTA's warps.
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// -------------------------------------------------------------------- launch
+// Launchers implemented in the kernel translation units. Each returns a
+// cudaError_t from the launch (cudaSuccess when nothing needed launching).
+struct SummarizeArgs {
+  const asp_paged_kv* kv;
+  int mode;
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  uint32_t* err;
+};
+cudaError_t launch_summarize(const SummarizeArgs& a, cudaStream_t stream);
+
+struct SelectArgs {
+  const asp_paged_kv* kv;
+  const float* q;
+  float gamma;
+  int budget;
+  int32_t* lists;
+  int32_t* lens;
+  float* scores;
+  uint32_t* err;
+  int num_sms;
+};
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream);
+
+struct DecodeArgs {
+  const asp_paged_kv* kv;
+  const float* q;
+  const int32_t* lists;
+  const int32_t* lens;
+  float sm_scale;
+  float* out;
+  float* lse;
+  float* partials;
+  int32_t* counters;
+  uint32_t* err;
+  int grid;
+  int slot_floats;
+};
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// Per-device helpers (abi.cu).
+int current_device_sm_count();
+cudaError_t set_max_dynamic_smem(const void* func, int bytes);
+
+}  // namespace asp

@@ -1,0 +1,558 @@
+// decode.cu - self-planning sparse attention over ragged page lists (MOIRA
+// abstract: each thread block derives its own share of the work from the
+// list lengths, so the decode step needs no host-side plan and stays inside
+// the CUDA graph).
+//
+// Plan (every CTA, on the device): load lens[B*Hkv] into shared memory and
+// take their inclusive prefix; the concatenated lists form one sequence of
+// `total` pages, and CTA c of G takes positions [c*total/G, (c+1)*total/G).
+// Shares differ by at most one page whatever the length mix. A CTA's range
+// cuts at most two segments; each (segment, CTA) piece produces one partial
+// (m, l, o) in slot segment + CTA of the workspace, which is unique because
+// both indices grow along the sequence. A per-segment counter elects the last
+// CTA to finish a segment; it merges the partials by log-sum-exp and resets
+// the counter, so nothing ever waits on another CTA.
+//
+// Data path (per CTA: 8 consumer warps + 1 producer warp, one CTA per SM):
+// the producer resolves list entry -> logical page -> physical page and
+// issues 2-D TMA loads of the page's K and V in 16-token sub-tiles ([16 rows x
+// 64 channels], 128-byte swizzle) into a shared-memory ring tracked by
+// mbarriers. Consumer warp w takes stages w, w+8, ... of the current piece and
+// keeps its own online-softmax state; the warps are merged in shared memory
+// at the end of each piece.
+//
+// Per page the contraction is small (g <= 8 queries against P tokens), so it
+// runs on mma.sync m16n8k16 bf16 with tokens as the M dimension and the query
+// group (padded to 8) as N:
+//   S^T[16 x 8] = K[16 x d] . Q^T[d x 8]      (Q split into bf16 hi + lo)
+//   O^T[d x 8] += V^T[d x 16] . P^T[16 x 8]   (probabilities rounded to bf16)
+// The S^T accumulator becomes the P^T operand through movmatrix.trans, and the
+// swizzled tiles make every ldmatrix conflict-free. A page is 4-32 KiB of HBM
+// against 4-8 flop per byte, far below any tensor-core limit: the kernel is
+// bound by HBM, and the 128 KiB ring keeps that much per SM in flight.
+#include "asp_internal.cuh"
+
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+namespace asp {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kDecWarps = 8;
+constexpr int kDecThreads = (kDecWarps + 1) * 32;
+constexpr int kRingBudget = 131072;  // bytes of the K/V ring
+
+// The ring is staged in 16-token sub-tiles of a page (P/16 stages per page),
+// so a stage is 8 KiB (d=128) or 4 KiB (d=64) for every page size. Stage `it`
+// goes to ring slot it % kStages and to consumer warp it % 8; with kStages a
+// multiple of 8 every slot belongs to one warp, which has consumed the slot's
+// previous use itself before it waits on the slot again. That keeps each
+// mbarrier at most one phase from its waiter, which parity waits require.
+template <int D, int P>
+struct Cfg {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kSubs = P / 16;                      // stages per page
+  static constexpr int kTileBytes = 16 * 128;               // [16 rows x 64 bf16], swizzled
+  static constexpr int kPartBytes = kHalves * kTileBytes;   // K (or V) of 16 tokens
+  static constexpr int kStageBytes = 2 * kPartBytes;        // K then V
+  static constexpr int kStages = kRingBudget / kStageBytes; // 16 (d=128) or 32 (d=64)
+  static_assert(kStages % kDecWarps == 0, "ring slots must be owned by single warps");
+  static constexpr int kMergeFloats = kDecWarps * (2 * 8 + 8 * D);
+  static constexpr int kSlotFloats = 2 * 8 + 8 * D;
+};
+
+struct DecParams {
+  const float* q;
+  const int32_t* lists;
+  const int32_t* lens;
+  const int32_t* bt;
+  const int32_t* seq_lens;
+  float* out;
+  float* lse;
+  float* partials;
+  int32_t* counters;
+  uint32_t* err;
+  int B, Hq, Hkv, g, max_pages, num_phys, slot_floats;
+  float scale_log2;
+};
+
+// ------------------------------------------------------------ mma helpers
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Byte offset of (row r < 16, channel c, c % 8 == 0) inside a stage's K or V
+// part, laid out as kHalves tiles of [16 rows x 128 B] with the 128-byte
+// swizzle (16-byte chunk index XOR row % 8; tiles start on 1 KiB boundaries).
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  const int hh = c >> 6, chunk = (c & 63) >> 3;
+  return hh * (16 * 128) + r * 128 + ((chunk ^ (r & 7)) << 4);
+}
+
+__device__ __forceinline__ int seg_of(const int* prefix, int S, int pos) {
+  int lo = 0, hi = S - 1;  // largest s with prefix[s] <= pos
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= pos) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// CTA whose range [c*total/G, (c+1)*total/G) holds position x.
+__device__ __forceinline__ int cta_of(long long x, long long total, int G) {
+  return (int)(((x + 1) * G - 1) / total);
+}
+
+template <int D, int P>
+__global__ void __launch_bounds__(kDecThreads, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const DecParams p) {
+  using C = Cfg<D, P>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  float* merge = reinterpret_cast<float*>(ring + C::kStages * C::kStageBytes);
+  int4* meta = reinterpret_cast<int4*>(merge + C::kMergeFloats);
+  uint64_t* full = reinterpret_cast<uint64_t*>(meta + C::kStages);
+  uint64_t* empty = full + C::kStages;
+  int* flags = reinterpret_cast<int*>(empty + C::kStages);  // [0] last-arriver, [1] warp sums...
+  int* prefix = flags + 48;                                  // [S + 1]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = p.B * p.Hkv;
+  const int G = gridDim.x, cta = blockIdx.x;
+
+  if (tid == 0) {
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_fence_init();
+    prefix[0] = 0;
+  }
+  // ---- self-plan: lengths (validated) -> inclusive prefix in shared memory
+  const int per = ceil_div(S, kDecThreads);
+  const int a0 = min(S, tid * per), a1 = min(S, a0 + per);
+  int run = 0;
+  for (int s = a0; s < a1; ++s) {
+    const int b = s / p.Hkv;
+    const int n_b = ceil_div(clamp_seq_len(p.seq_lens[b], p.max_pages, P, p.err), P);
+    int n = p.lens[s];
+    if (n < 0 || n > n_b) {
+      report(p.err, ASP_DEVERR_LEN_RANGE);
+      n = n < 0 ? 0 : n_b;
+    }
+    run += n;
+    prefix[s + 1] = run;
+  }
+  int x = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) flags[8 + warp] = x;
+  __syncthreads();
+  int off = 0;
+  for (int w = 0; w < warp; ++w) off += flags[8 + w];
+  off += x - run;
+  for (int s = a0; s < a1; ++s) prefix[s + 1] += off;
+  __syncthreads();
+
+  const long long total = prefix[S];
+  const int geff = (int)(total < G ? total : G);
+  long long beg = 0, end = 0;
+  if (cta < geff) {
+    beg = (long long)cta * total / geff;
+    end = (long long)(cta + 1) * total / geff;
+  }
+
+  if (warp == kDecWarps) {
+    // =============================================================== producer
+    if (beg >= end) return;
+    if (lane == 0) {
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+    }
+    bool aborted = false;
+    int issued = 0;
+    for (long long base = beg; base < end && !aborted; base += 32) {
+      const long long pos = base + lane;
+      int ok = 0, row = 0, ntok = 0, lp = -1;
+      if (pos < end) {
+        const int s = seg_of(prefix, S, (int)pos);
+        const int b = s / p.Hkv, h = s % p.Hkv;
+        const int T = clamp_seq_len(p.seq_lens[b], p.max_pages, P, nullptr);
+        const int n_b = ceil_div(T, P);
+        lp = __ldg(p.lists + (size_t)s * p.max_pages + (int)(pos - prefix[s]));
+        if (lp < 0 || lp >= n_b) {
+          report(p.err, ASP_DEVERR_LIST_RANGE);
+        } else {
+          const int phys = __ldg(p.bt + (size_t)b * p.max_pages + lp);
+          if (phys < 0 || phys >= p.num_phys) {
+            report(p.err, ASP_DEVERR_PAGE_RANGE);
+          } else {
+            ok = 1;
+            row = (phys * p.Hkv + h) * P;
+            ntok = min(P, T - lp * P);
+          }
+        }
+      }
+      const int nb = (int)min(32LL, end - base);
+      for (int i = 0; i < nb && !aborted; ++i) {
+        const int r_ok = __shfl_sync(kFull, ok, i);
+        const int r_row = __shfl_sync(kFull, row, i);
+        const int r_ntok = __shfl_sync(kFull, ntok, i);
+        const int r_lp = __shfl_sync(kFull, lp, i);
+#pragma unroll 1
+        for (int sub = 0; sub < C::kSubs; ++sub) {
+          // stage `it` = 16-token sub-tile `sub` of the page at position base + i
+          const int it = (int)(base + i - beg) * C::kSubs + sub;
+          const int stage = it % C::kStages;
+          const int sub_ntok = min(16, max(0, r_ntok - 16 * sub));
+          if (lane == 0) {
+            if (!mbar_wait(&empty[stage], ((it / C::kStages) & 1) ^ 1)) {
+              report(p.err, ASP_DEVERR_TIMEOUT);
+              aborted = true;
+            } else {
+              const bool load = r_ok && sub_ntok > 0;
+              meta[stage] = make_int4(r_lp, sub_ntok, load ? 1 : 0, 0);
+              uint8_t* dst = ring + stage * C::kStageBytes;
+              if (load) {
+                mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+#pragma unroll
+                for (int hh = 0; hh < C::kHalves; ++hh) {
+                  tma_load_2d(dst + hh * C::kTileBytes, &tmK, hh * 64, r_row + 16 * sub,
+                              &full[stage]);
+                  tma_load_2d(dst + C::kPartBytes + hh * C::kTileBytes, &tmV, hh * 64,
+                              r_row + 16 * sub, &full[stage]);
+                }
+              } else {
+                mbar_arrive(&full[stage]);
+              }
+              ++issued;
+            }
+          }
+          aborted = __shfl_sync(kFull, aborted ? 1 : 0, 0) != 0;
+          if (aborted) break;
+        }
+      }
+    }
+    issued = __shfl_sync(kFull, issued, 0);
+    if (lane == 0)  // never leave the CTA with copies in flight
+      for (int it = max(0, issued - C::kStages); it < issued; ++it)
+        mbar_wait(&full[it % C::kStages], (it / C::kStages) & 1);
+    return;
+  }
+
+  // ================================================================ consumers
+  const int ctid = tid;  // 0..255
+  const int gid = lane >> 2, tq = lane & 3;
+  const float kLn2 = 0.69314718055994530942f;
+
+  // segments with an empty list: out = 0, lse = -inf
+  for (int s = cta; s < S; s += G) {
+    if (prefix[s + 1] != prefix[s]) continue;
+    const int b = s / p.Hkv, h = s % p.Hkv;
+    for (int e = ctid; e < p.g * D; e += kDecWarps * 32)
+      p.out[((size_t)b * p.Hq + h * p.g + e / D) * D + e % D] = 0.f;
+    for (int e = ctid; e < p.g; e += kDecWarps * 32)
+      p.lse[(size_t)b * p.Hq + h * p.g + e] = -INFINITY;
+  }
+  if (beg >= end) return;
+
+  bool aborted = false;
+  long long pos = beg;
+  while (pos < end) {
+    const int s = seg_of(prefix, S, (int)pos);
+    const long long seg_lo = prefix[s], seg_hi = prefix[s + 1];
+    const long long pe = seg_hi < end ? seg_hi : end;
+    const int b = s / p.Hkv, h = s % p.Hkv;
+
+    // Q^T fragments (B operand): rows d = kk*16 + 2*tq (+1, +8, +9), column gid
+    uint32_t qhi[D / 16][2], qlo[D / 16][2];
+    {
+      const bool live = gid < p.g;
+      const float* qr = p.q + ((size_t)b * p.Hq + h * p.g + (live ? gid : 0)) * D;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float2 v = make_float2(0.f, 0.f);
+          if (live) v = *reinterpret_cast<const float2*>(qr + kk * 16 + half * 8 + 2 * tq);
+          v.x *= p.scale_log2;
+          v.y *= p.scale_log2;
+          const __nv_bfloat162 hv = __floats2bfloat162_rn(v.x, v.y);
+          const float2 hf = __bfloat1622float2(hv);
+          qhi[kk][half] = *reinterpret_cast<const uint32_t*>(&hv);
+          qlo[kk][half] = pack_bf16(v.x - hf.x, v.y - hf.y);
+        }
+    }
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float o[D / 16][4];
+#pragma unroll
+    for (int dt = 0; dt < D / 16; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+
+    const int it0 = (int)(pos - beg) * C::kSubs, it1 = (int)(pe - beg) * C::kSubs;
+    for (int it = it0 + ((warp - it0) % kDecWarps + kDecWarps) % kDecWarps; it < it1;
+         it += kDecWarps) {
+      const int stage = it % C::kStages;
+      if (!aborted && !mbar_wait(&full[stage], (it / C::kStages) & 1)) {
+        if (lane == 0) report(p.err, ASP_DEVERR_TIMEOUT);
+        aborted = true;
+      }
+      const int4 mt = meta[stage];
+      if (!aborted && mt.z) {
+        const int ntok = mt.y;
+        const uint32_t kb = smem_u32(ring + stage * C::kStageBytes);
+        const uint32_t vb = kb + C::kPartBytes;
+        const int j = lane >> 3;
+        // ---- S^T[16 x 8] = K[16 x d] . Q^T[d x 8]
+        float sv[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+          const int r = (j & 1) * 8 + (lane & 7);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            uint32_t a[4];
+            ldsm_x4(kb + swz(r, kk * 16 + (j >> 1) * 8), a);
+            mma16816(sv, a, qhi[kk][0], qhi[kk][1]);
+            mma16816(sv, a, qlo[kk][0], qlo[kk][1]);
+          }
+        }
+        // ---- mask tokens past the sequence, online softmax (log2 domain)
+        if (gid >= ntok) sv[0] = sv[1] = -INFINITY;
+        if (gid + 8 >= ntok) sv[2] = sv[3] = -INFINITY;
+        float cm0 = fmaxf(sv[0], sv[2]), cm1 = fmaxf(sv[1], sv[3]);
+#pragma unroll
+        for (int off2 = 4; off2 < 32; off2 <<= 1) {
+          cm0 = fmaxf(cm0, __shfl_xor_sync(kFull, cm0, off2));
+          cm1 = fmaxf(cm1, __shfl_xor_sync(kFull, cm1, off2));
+        }
+        const float n0 = fmaxf(m0, cm0), n1 = fmaxf(m1, cm1);
+        const float al0 = exp2f(m0 - n0), al1 = exp2f(m1 - n1);
+        m0 = n0;
+        m1 = n1;
+#pragma unroll
+        for (int dt = 0; dt < D / 16; ++dt) {
+          o[dt][0] *= al0;
+          o[dt][1] *= al1;
+          o[dt][2] *= al0;
+          o[dt][3] *= al1;
+        }
+        const float p0 = exp2f(sv[0] - n0), p1 = exp2f(sv[1] - n1);
+        const float p2 = exp2f(sv[2] - n0), p3 = exp2f(sv[3] - n1);
+        l0 = l0 * al0 + (p0 + p2);
+        l1 = l1 * al1 + (p1 + p3);
+        const uint32_t pb0 = movm_t(pack_bf16(p0, p1));
+        const uint32_t pb1 = movm_t(pack_bf16(p2, p3));
+        // ---- rows past the sequence may hold anything: zero them in V
+        if (ntok < 16) {
+          uint8_t* vpart = ring + stage * C::kStageBytes + C::kPartBytes;
+          const int chunks = (16 - ntok) * C::kHalves * 8;
+          for (int e = lane; e < chunks; e += 32) {
+            const int r = ntok + e / (C::kHalves * 8);
+            const int hh = (e / 8) % C::kHalves;
+            *reinterpret_cast<uint4*>(vpart + hh * C::kTileBytes + r * 128 + (e % 8) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        // ---- O^T[d x 8] += V^T[d x 16] . P^T[16 x 8]
+        {
+          const int r = (j >> 1) * 8 + (lane & 7);
+#pragma unroll
+          for (int dt = 0; dt < D / 16; ++dt) {
+            uint32_t a[4];
+            ldsm_x4_t(vb + swz(r, dt * 16 + (j & 1) * 8), a);
+            mma16816(o[dt], a, pb0, pb1);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+    }
+
+    // ---- merge the 8 warps' states of this piece
+#pragma unroll
+    for (int off2 = 4; off2 < 32; off2 <<= 1) {
+      l0 += __shfl_xor_sync(kFull, l0, off2);
+      l1 += __shfl_xor_sync(kFull, l1, off2);
+    }
+    float* mw = merge + warp * C::kSlotFloats;  // m[8], l[8], o[8][D]
+    if (gid == 0) {
+      mw[2 * tq] = m0;
+      mw[2 * tq + 1] = m1;
+      mw[8 + 2 * tq] = l0;
+      mw[8 + 2 * tq + 1] = l1;
+    }
+#pragma unroll
+    for (int dt = 0; dt < D / 16; ++dt) {
+      const int d0 = dt * 16 + gid;
+      mw[16 + (2 * tq) * D + d0] = o[dt][0];
+      mw[16 + (2 * tq + 1) * D + d0] = o[dt][1];
+      mw[16 + (2 * tq) * D + d0 + 8] = o[dt][2];
+      mw[16 + (2 * tq + 1) * D + d0 + 8] = o[dt][3];
+    }
+    named_bar_sync(1, kDecWarps * 32);
+    const bool whole = (pos == seg_lo) && (pe == seg_hi);
+    float* slot = p.partials + (size_t)(s + cta) * p.slot_floats;
+    for (int e = ctid; e < p.g * D; e += kDecWarps * 32) {
+      const int col = e / D, d = e % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, merge[w * C::kSlotFloats + col]);
+      float L = 0.f, acc = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kDecWarps; ++w) {
+          const float* q = merge + w * C::kSlotFloats;
+          const float sc = exp2f(q[col] - M);
+          L += sc * q[8 + col];
+          acc += sc * q[16 + col * D + d];
+        }
+      }
+      if (whole) {
+        const size_t row = (size_t)b * p.Hq + h * p.g + col;
+        p.out[row * D + d] = L > 0.f ? acc / L : 0.f;
+        if (d == 0) p.lse[row] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+      } else {
+        slot[16 + col * D + d] = acc;
+        if (d == 0) {
+          slot[col] = M;
+          slot[8 + col] = L;
+        }
+      }
+    }
+    if (!whole) {
+      __threadfence();
+      named_bar_sync(1, kDecWarps * 32);
+      if (ctid == 0) {
+        const int cf = cta_of(seg_lo, total, geff), cl = cta_of(seg_hi - 1, total, geff);
+        const int prev = atomicAdd(&p.counters[s], 1);
+        const int last = prev == cl - cf;
+        if (last) p.counters[s] = 0;
+        flags[0] = last ? 1 : 0;
+        flags[1] = cf;
+        flags[2] = cl;
+      }
+      named_bar_sync(1, kDecWarps * 32);
+      if (flags[0]) {
+        __threadfence();
+        const int cf = flags[1], cl = flags[2];
+        for (int e = ctid; e < p.g * D; e += kDecWarps * 32) {
+          const int col = e / D, d = e % D;
+          float M = -INFINITY;
+          for (int c = cf; c <= cl; ++c)
+            M = fmaxf(M, __ldcg(p.partials + (size_t)(s + c) * p.slot_floats + col));
+          float L = 0.f, acc = 0.f;
+          if (M != -INFINITY) {
+            for (int c = cf; c <= cl; ++c) {
+              const float* q = p.partials + (size_t)(s + c) * p.slot_floats;
+              const float sc = exp2f(__ldcg(q + col) - M);
+              L += sc * __ldcg(q + 8 + col);
+              acc += sc * __ldcg(q + 16 + col * D + d);
+            }
+          }
+          const size_t row = (size_t)b * p.Hq + h * p.g + col;
+          p.out[row * D + d] = L > 0.f ? acc / L : 0.f;
+          if (d == 0) p.lse[row] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+        }
+      }
+    }
+    named_bar_sync(1, kDecWarps * 32);  // merge area is rewritten by the next piece
+    pos = pe;
+  }
+}
+
+// ----------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// [rows = num_phys*Hkv*P, D] bf16 viewed as 2-D; box = [16 rows x 64 channels].
+cudaError_t make_page_map(CUtensorMap* map, const void* base, long long rows, int D, int P) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  cuuint32_t box[2] = {64, 16};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int D, int P>
+cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
+  using C = Cfg<D, P>;
+  const asp_paged_kv& kv = *a.kv;
+  const int S = kv.batch * kv.num_kv_heads;
+  const size_t smem = 1024 + (size_t)C::kStages * C::kStageBytes + C::kMergeFloats * 4 +
+                      C::kStages * sizeof(int4) + 2 * C::kStages * 8 + 48 * 4 + (S + 1) * 4;
+  cudaError_t e = set_max_dynamic_smem((const void*)decode_kernel<D, P>, (int)smem);
+  if (e != cudaSuccess) return e;
+  const long long rows = (long long)kv.num_phys_pages * kv.num_kv_heads * P;
+  CUtensorMap tk, tv;
+  if ((e = make_page_map(&tk, kv.k_cache, rows, D, P)) != cudaSuccess) return e;
+  if ((e = make_page_map(&tv, kv.v_cache, rows, D, P)) != cudaSuccess) return e;
+  DecParams p{a.q, a.lists, a.lens, kv.block_table, kv.seq_lens, a.out, a.lse, a.partials,
+              a.counters, a.err, kv.batch, kv.num_q_heads, kv.num_kv_heads,
+              kv.num_q_heads / kv.num_kv_heads, kv.max_pages, kv.num_phys_pages, a.slot_floats,
+              a.sm_scale * 1.4426950408889634f};
+  decode_kernel<D, P><<<a.grid, kDecThreads, smem, stream>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+  const int d = a.kv->head_dim, P = a.kv->page_size;
+  if (d == 128 && P == 16) return launch_decode_t<128, 16>(a, stream);
+  if (d == 128 && P == 32) return launch_decode_t<128, 32>(a, stream);
+  if (d == 128 && P == 64) return launch_decode_t<128, 64>(a, stream);
+  if (d == 64 && P == 16) return launch_decode_t<64, 16>(a, stream);
+  if (d == 64 && P == 32) return launch_decode_t<64, 32>(a, stream);
+  if (d == 64 && P == 64) return launch_decode_t<64, 64>(a, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace asp

@@ -1,0 +1,470 @@
+#!/usr/bin/env python3
+"""Decode-step benchmark: coverage-selected sparse attention over a paged KV cache.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl asp|reference]
+                    [--config long128k] [--gamma 0.99]
+
+One step = every layer of the workload through asp_coverage_select (score +
+select kernels) and asp_sparse_decode, replayed from one CUDA graph, with all
+inputs resident in HBM (64 GiB of K/V at 128k: far larger than L2, so no L2
+flush is needed between steps). Prints one JSON line (rank 0).
+
+Under torchrun each rank runs its own batch of requests (the path shards by
+request with no collective); value = all ranks' steps / max-over-ranks time.
+
+--impl reference times the fp64 CPU oracle (numpy, spawn pool over the host
+cores) on a bounded sample of the same workload and scales it to steps/s.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import multiprocessing as mp
+import os
+import re
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode steps/s and selected-KV HBM GB/s (% of GB300 roofline) at 128k, γ=0.99"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ helpers
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["asp", "reference"], default="asp")
+    ap.add_argument("--config", default="long128k")
+    ap.add_argument("--gamma", type=float, default=0.99)
+    ap.add_argument("--seed", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-dense", action="store_true")
+    ap.add_argument("--oracle-segments", type=int, default=0,
+                    help="segments per oracle sample (default: host cores, at least 8)")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def max_over_ranks(x: float, dist, device=None) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_traffic_per_page(cfg_name: str):
+    """ncu DRAM bytes per selected (page, head) of the decode kernel, if the
+    committed profile was taken on the current kernel source; else None."""
+    src = os.path.join(ROOT, "adaptive_sparse_paged_gb300", "csrc", "decode.cu")
+    path = os.path.join(ROOT, "profiles", "decode_kernel_ncu.md")
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        text = open(path).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"decode\.cu sha256\[:16\]:\s*([0-9a-f]{16})", text)
+    m_val = re.search(r"dram bytes per selected page-head:\s*([0-9.]+)", text)
+    if not m_hash or not m_val or m_hash.group(1) != digest:
+        return None
+    return float(m_val.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.proc.stdout.readline()  # first sample: the sampler is running
+        except (OSError, ValueError):
+            self.proc = None
+
+    def mark(self, which):
+        if which == 0:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append(parts)
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        smax = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i] == "Active"})
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((float(r[4]) for r in rows
+                                    if r[4].replace(".", "").isdigit()), default=None)}
+
+
+# ------------------------------------------------------------- oracle sample
+def _oracle_worker(args):
+    import numpy as np
+    import oracle.asp_oracle as O
+    qg, kbits, vbits, T, gamma, budget, scale = args
+    kp = O.bf16_bits_to_f64(kbits)
+    vp = O.bf16_bits_to_f64(vbits)
+    r = O.decode_segment(qg, kp, vp, T, gamma, budget, scale)
+    return int(len(r["ids"])), float(np.abs(r["o"]).sum())
+
+
+def _pool_init():
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+
+
+def start_oracle_pool():
+    n = os.cpu_count() or 1
+    os.environ["OMP_NUM_THREADS"] = "1"
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    os.environ["MKL_NUM_THREADS"] = "1"
+    ctx = mp.get_context("spawn")
+    return ctx.Pool(n, initializer=_pool_init), n
+
+
+def oracle_sample_tasks(w, sh, layer, nseg, gamma, budget, seed):
+    """Seeded sample of (request, KV head) segments of one layer, as oracle inputs."""
+    import numpy as np
+    import torch
+    rng = np.random.default_rng(seed)
+    segs = [(b, h) for b in range(w.batch) for h in range(w.num_kv_heads)]
+    pick = [segs[i] for i in rng.choice(len(segs), min(nseg, len(segs)), replace=False)]
+    g = w.num_q_heads // w.num_kv_heads
+    q = layer.q.double().cpu().numpy()
+    tasks = []
+    for b, h in pick:
+        T = int(sh.seq_lens[b])
+        n = sh.num_pages[b]
+        idx = sh.block_table[b, :n].long()
+        kb = layer.k_cache[idx, h].contiguous().view(torch.int16).cpu().numpy()
+        vb = layer.v_cache[idx, h].contiguous().view(torch.int16).cpu().numpy()
+        tasks.append((q[b, h * g:(h + 1) * g], kb, vb, T, gamma, budget,
+                      1.0 / math.sqrt(w.head_dim)))
+    return tasks
+
+
+def time_oracle(pool, tasks):
+    t0 = time.perf_counter()
+    pool.map(_oracle_worker, tasks, chunksize=1)
+    return time.perf_counter() - t0
+
+
+# ------------------------------------------------------------------- asp arm
+def run_asp(args):
+    world, rank, local = dist_env()
+    pool = cores = None
+    if rank == 0 and not args.no_cpu_baseline:
+        pool, cores = start_oracle_pool()  # spawn, before any CUDA call
+    import numpy as np
+    import torch
+
+    from adaptive_sparse_paged_gb300 import binding as B
+    from adaptive_sparse_paged_gb300 import synth
+    from adaptive_sparse_paged_gb300.step import DecodeStep
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = dist_init(world, "nccl")
+    w = synth.CONFIGS[args.config]
+    seed = args.seed + 1000 * rank
+    t_gen = time.perf_counter()
+    sh = synth.make_shared(w, seed, dev)
+    layers, kvs = [], []
+    for l in range(w.layers):
+        lay = synth.make_layer(w, sh, seed, l, dev)
+        summ = torch.empty((sh.num_phys_pages, w.num_kv_heads, 2, w.head_dim),
+                           dtype=torch.bfloat16, device=dev)
+        kv = B.PagedKV(lay.k_cache, lay.v_cache, summ, sh.block_table, sh.seq_lens, w.num_q_heads)
+        layers.append(lay)
+        kvs.append(kv)
+    q_all = torch.stack([lay.q for lay in layers])
+    ws0 = B.new_workspace(kvs[0])
+    for kv in kvs:
+        B.asp_page_summarize(kv, B.ASP_SUMMARIZE_BULK, None, None, ws0)
+    assert B.asp_get_device_error(ws0) == 0
+    torch.cuda.synchronize()
+    gen_s = time.perf_counter() - t_gen
+
+    step = DecodeStep(kvs, q_all, gamma=args.gamma)
+    step.capture()
+    stream = torch.cuda.current_stream()
+
+    def timed_graph(st, K, W):
+        for _ in range(W):
+            st.replay()
+        torch.cuda.synchronize()
+        barrier(dist)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            st.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+        return e0.elapsed_time(e1) / 1e3
+
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    clocks.mark(0)
+    t_loc = timed_graph(step, args.steps, max(3, args.warmup))
+    clocks.mark(1)
+    clk = clocks.stop()
+    t_max = max_over_ranks(t_loc, dist, dev)
+    assert B.asp_get_device_error(step.ws) == 0
+
+    # selection statistics of this step (same every replay)
+    lens = step.lens.cpu().numpy().astype(np.int64)     # [L, B, Hkv]
+    n_pages = np.array(sh.num_pages, dtype=np.int64)     # [B]
+    sel_pages = int(lens.sum())
+    all_pages = int(n_pages.sum()) * w.num_kv_heads * w.layers
+    P, d, Hq, Hkv, Bt, L = w.page_size, w.head_dim, w.num_q_heads, w.num_kv_heads, w.batch, w.layers
+    page_bytes = 2 * P * d * 2                        # K + V of one (page, head)
+    q_bytes = Bt * Hq * d * 4
+    out_bytes = Bt * Hq * d * 4 + Bt * Hq * 4
+    dec_bytes = [int(lens[l].sum()) * (page_bytes + 8) + q_bytes + Bt * Hkv * 4 + out_bytes
+                 for l in range(L)]                  # pages + list/table entries + q + lens + out
+    score_bytes = int(n_pages.sum()) * (Hkv * 4 * d + 4) + q_bytes   # summaries + table + q
+    select_bytes = [int(lens[l].sum()) * 4 + Bt * Hkv * 4 for l in range(L)]
+    step_bytes = sum(dec_bytes) + L * score_bytes + sum(select_bytes)
+
+    # per-kernel durations: eager pass with events on the launching stream
+    K_e = max(3, min(args.steps, 20))
+    for _ in range(2):
+        step.run()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(L * K_e)]
+    for k in range(K_e):
+        for l in range(L):
+            step.run_layer(l, stream, events=evs[k * L + l])
+    torch.cuda.synchronize()
+    sel_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(L * K_e)]
+    dec_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(L * K_e)]
+    dec_avg_s = float(np.mean(dec_ms)) / 1e3
+    sel_avg_s = float(np.mean(sel_ms)) / 1e3
+    dec_bytes_avg = float(np.mean(dec_bytes))
+    peak, peak_kind = measured_hbm_peak()
+    dec_gbs = dec_bytes_avg / dec_avg_s / 1e9
+    tpp = decode_traffic_per_page(args.config)
+    traffic = None if tpp is None else tpp * float(lens.sum()) / L
+
+    # dense comparison: the same kernels at gamma = 1
+    dense = None
+    if not args.no_dense:
+        dstep = DecodeStep(kvs, q_all, gamma=1.0)
+        dstep.capture()
+        Kd = max(3, args.steps // 4)
+        td = max_over_ranks(timed_graph(dstep, Kd, 3), dist, dev)
+        dense = {"steps_per_s": world * Kd / td, "ms_per_step": 1e3 * td / Kd}
+        del dstep
+
+    # end to end: host q in, host out/lse back, every step
+    q_host = q_all.cpu().pin_memory()
+    out_host = torch.empty(step.out.shape, dtype=torch.float32).pin_memory()
+    lse_host = torch.empty(step.lse.shape, dtype=torch.float32).pin_memory()
+    K2 = args.steps
+    for _ in range(3):
+        step.q.copy_(q_host, non_blocking=True)
+        step.replay()
+        out_host.copy_(step.out, non_blocking=True)
+        lse_host.copy_(step.lse, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(dist)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K2):
+        step.q.copy_(q_host, non_blocking=True)
+        step.replay()
+        out_host.copy_(step.out, non_blocking=True)
+        lse_host.copy_(step.lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, dist, dev)
+    e2e = {"value": world * K2 / t_e2e, "unit": "steps/s",
+           "h2d_bytes_per_step": int(q_host.numel() * 4),
+           "d2h_bytes_per_step": int(out_host.numel() * 4 + lse_host.numel() * 4)}
+
+    cpu = None
+    if pool is not None:
+        nseg = args.oracle_segments or max(8, cores)
+        tasks = oracle_sample_tasks(w, sh, layers[0], nseg, args.gamma, 0, args.seed)
+        time_oracle(pool, tasks[:min(len(tasks), cores)])  # warm the workers
+        t_cpu = time_oracle(pool, tasks)
+        segs_per_step = w.batch * w.num_kv_heads * w.layers
+        step_s = t_cpu * segs_per_step / len(tasks)
+        cpu = {"value": 1.0 / step_s, "unit": "steps/s", "cores": cores, "kind": "oracle",
+               "sample": f"{len(tasks)} of {segs_per_step} (request, KV head, layer) segments "
+                         f"of layer 0, full context each, fp64 numpy, {cores} spawn workers "
+                         f"x 1 thread; {t_cpu:.1f} s scaled to a full step"}
+        pool.close()
+
+    if rank == 0:
+        steps_per_s = world * args.steps / t_max
+        ms = 1e3 * t_max / args.steps
+        line = {
+            "metric": METRIC,
+            "value": round(steps_per_s, 3),
+            "unit": "steps/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": max(3, args.warmup),
+            "ms_per_step": round(ms, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic",
+            "config": {
+                "workload": f"{w.name}: B{w.batch} L{w.layers} Hq{Hq} Hkv{Hkv} d{d} P{P} "
+                            f"T{w.seq_len or 'lognormal'} gamma{args.gamma}, one CUDA graph per step",
+                "gamma": args.gamma,
+                "l2": "inputs larger than L2 (K/V %.1f GiB, summaries %.2f GiB resident); no flush"
+                      % (2 * sh.num_phys_pages * Hkv * P * d * 2 * L / 2**30,
+                         sh.num_phys_pages * Hkv * 4 * d * L / 2**30),
+                "parallelism": f"replica per GPU x{world} (requests shard, no collective)",
+                "setup_s": round(gen_s, 1),
+            },
+            "selected_kv_gbs": round(world * step_bytes * args.steps / t_max / 1e9, 1),
+            "hbm_frac_of_measured": round(step_bytes / (ms / 1e3) / 1e9 / peak, 4),
+            "hbm_frac_of_nominal_8tbs": round(step_bytes / (ms / 1e3) / 1e12 / 8.0, 4),
+            "pages_read_frac": round(sel_pages / all_pages, 4),
+            "bytes_per_step": step_bytes,
+            "dense_gamma1": dense,
+            "kernels_ms": {"select_avg": round(sel_avg_s * 1e3, 4),
+                           "decode_avg": round(dec_avg_s * 1e3, 4)},
+            "roofline": {
+                "kernel": "decode_kernel (asp_sparse_decode)",
+                "bound": "hbm",
+                "achieved": round(dec_gbs, 1),
+                "peak": peak,
+                "peak_kind": peak_kind,
+                "unit": "GB/s",
+                "frac": round(dec_gbs / peak, 4),
+                "traffic": None if traffic is None else round(traffic),
+                "algorithmic_bytes_per_launch": round(dec_bytes_avg),
+            },
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps * step.launches_per_step,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------- reference arm
+def run_reference(args):
+    world, rank, local = dist_env()
+    if rank != 0:
+        return  # the oracle arm runs once, on rank 0's host
+    pool, cores = start_oracle_pool()
+    import torch
+
+    from adaptive_sparse_paged_gb300 import synth
+    w = synth.CONFIGS[args.config]
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    sh = synth.make_shared(w, args.seed, dev)
+    lay = synth.make_layer(w, sh, args.seed, 0, dev)
+    nseg = args.oracle_segments or max(8, cores)
+    segs_per_step = w.batch * w.num_kv_heads * w.layers
+    tasks = oracle_sample_tasks(w, sh, lay, nseg, args.gamma, 0, args.seed)
+    del lay
+    for _ in range(max(0, min(args.warmup, 1))):
+        time_oracle(pool, tasks[:min(len(tasks), cores)])
+    t = 0.0
+    for _ in range(args.steps):
+        t += time_oracle(pool, tasks) * segs_per_step / len(tasks)
+    pool.close()
+    value = args.steps / t
+    line = {
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": f"{w.name}: B{w.batch} L{w.layers} Hq{w.num_q_heads} "
+                               f"Hkv{w.num_kv_heads} d{w.head_dim} P{w.page_size} "
+                               f"T{w.seq_len or 'lognormal'} gamma{args.gamma}",
+                   "gamma": args.gamma},
+        "cpu_baseline": {"value": value, "unit": "steps/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: {len(tasks)} of {segs_per_step} segments of "
+                                   f"layer 0 through the fp64 oracle, scaled to a full step"},
+        "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_asp(args)
+
+
+if __name__ == "__main__":
+    main()

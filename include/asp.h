@@ -1,0 +1,205 @@
+/*
+ * asp.h - C ABI of the coverage-selected sparse paged decode library (libasp.so).
+ *
+ * One decode step of long-context attention reads, for every (request, layer,
+ * KV head), only the pages that a coverage rule selects: the smallest set of
+ * pages whose estimated attention mass reaches a fraction gamma. Attention then
+ * runs over those ragged per-head page lists, with every thread block deriving
+ * its own share of the work from the list lengths on the device, so that a
+ * whole step can be captured in one CUDA graph with no host-side plan.
+ *
+ * Sources: the MOIRA abstract on the page "Adaptive DHiSparse: Speculative
+ * Decoding over a Load-Adaptive KV Hierarchy" (thelatestinai.com/papers/
+ * 2610.13708) defines the coverage rule, the per-(request, layer, KV head,
+ * step) page lists and self-planning attention. The page estimate is a
+ * Quest-style bound; Quest is named in the abstract on the page "HiSparse:
+ * scaling sparse attention decoding with hierarchical KV cache"
+ * (scholarbro.com/p/47450-...). The pages print no interface: the calls below
+ * are this library's own.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Pointers: every tensor pointer is a DEVICE pointer (cudaMalloc'd or
+ *   equivalent) that the caller owns. The library never allocates or frees
+ *   memory and never synchronises inside the hot calls (asp_page_summarize,
+ *   asp_coverage_select, asp_sparse_decode), so they may be captured into a
+ *   CUDA graph. All work is enqueued on `stream`.
+ * - bf16 tensors are passed as uint16_t bit patterns.
+ * - Errors: arguments are checked on the host before any launch; a bad one
+ *   returns a negative asp_status and launches nothing. Problems that only
+ *   the device can see (an out-of-range block-table or list entry, a length
+ *   beyond the request) set bits in a sticky device error word inside the
+ *   workspace; the kernel then skips the offending page or clamps the length
+ *   and never traps. Read and clear the word with asp_get_device_error.
+ * - Shapes supported: head_dim d in {64, 128}; page_size P in {16, 32, 64};
+ *   num_kv_heads Hkv in {1, 2, 4, 8}; GQA group g = Hq / Hkv in {1, 2, 4, 8};
+ *   batch * Hkv <= 4096 segments; max_pages <= 1<<20. Anything else returns
+ *   ASP_EUNSUPPORTED.
+ * - The current CUDA device when a call is made must be the device that owns
+ *   the pointers.
+ */
+#ifndef ASP_H_
+#define ASP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ASP_ABI_VERSION 1
+
+typedef enum asp_status {
+  ASP_OK = 0,
+  ASP_EINVAL = -1,        /* null pointer, bad gamma/budget/scale, inconsistent sizes */
+  ASP_EUNSUPPORTED = -2,  /* shape outside the supported set listed above */
+  ASP_EWORKSPACE = -3,    /* workspace pointer null, misaligned (256 B) or too small */
+  ASP_ECUDA = -4,         /* a CUDA runtime call or kernel launch failed */
+  ASP_EDEVICE = -5        /* asp_get_device_error found a non-zero device error word */
+} asp_status;
+
+/* Bits of the device error word (see asp_get_device_error). */
+#define ASP_DEVERR_PAGE_RANGE 0x1u /* block_table entry outside [0, num_phys_pages): page skipped */
+#define ASP_DEVERR_LIST_RANGE 0x2u /* lists entry outside [0, N_b): page skipped */
+#define ASP_DEVERR_LEN_RANGE 0x4u  /* lens[b,h] outside [0, N_b]: clamped */
+#define ASP_DEVERR_SEQ_RANGE 0x8u  /* seq_lens[b] outside [0, max_pages*P]: clamped */
+#define ASP_DEVERR_TIMEOUT 0x10u   /* a bounded on-chip wait ran out: the kernel stopped early */
+
+/* A cudaStream_t, passed as an opaque pointer. NULL is the legacy default stream. */
+typedef void* asp_stream;
+
+/*
+ * Paged KV cache of ONE layer, plus its page summaries.
+ *
+ *   k_cache, v_cache : bf16 [num_phys_pages, Hkv, P, d]. The (page, head) block
+ *                      of P*d values is contiguous. Only asp_page_summarize in
+ *                      APPEND mode writes them.
+ *   summaries        : bf16 [num_phys_pages, Hkv, 2, d]; row 0 is the channel
+ *                      minimum of K over the page's valid tokens, row 1 the
+ *                      maximum. Written by asp_page_summarize, read by
+ *                      asp_coverage_select.
+ *   block_table      : int32 [batch, max_pages]; entry (b, p) is the physical
+ *                      page holding logical page p of request b. Shared by all
+ *                      heads and layers. Only entries p < N_b are read.
+ *   seq_lens         : int32 [batch]; T_b, the tokens of request b (counting the
+ *                      token being decoded). N_b = ceil(T_b / P) pages; the last
+ *                      page is partial when T_b % P != 0.
+ *   query head h uses KV head h / g (the group's heads are contiguous).
+ */
+typedef struct asp_paged_kv {
+  uint16_t* k_cache;
+  uint16_t* v_cache;
+  uint16_t* summaries;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int32_t batch;          /* B */
+  int32_t num_q_heads;    /* Hq */
+  int32_t num_kv_heads;   /* Hkv */
+  int32_t head_dim;       /* d */
+  int32_t page_size;      /* P (tokens per page) */
+  int32_t max_pages;      /* columns of block_table and of the page lists */
+  int32_t num_phys_pages; /* rows of k_cache / v_cache / summaries */
+} asp_paged_kv;
+
+/* Library ABI version (ASP_ABI_VERSION of the build). */
+int32_t asp_abi_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char* asp_status_string(asp_status status);
+
+/*
+ * Workspace bytes needed by asp_coverage_select / asp_sparse_decode /
+ * asp_page_summarize for this shape on the CURRENT device (the decode grid
+ * is sized from its SM count). Writes the size to *bytes. The workspace is a
+ * caller-owned device buffer, 256-byte aligned, that must be zeroed once with
+ * asp_workspace_init before first use; after that every call leaves it ready
+ * for the next (its counters return to zero), including under graph replay.
+ * Calls that share one workspace must be ordered on one stream.
+ */
+asp_status asp_workspace_size(const asp_paged_kv* kv, size_t* bytes);
+
+/* Zeroes the workspace's error word and counters (async on `stream`). */
+asp_status asp_workspace_init(void* ws, size_t ws_bytes, asp_stream stream);
+
+/*
+ * Page summaries: channel-wise min and max of K per (page, KV head).
+ * Definition: the Quest page summary used by the estimate of the coverage
+ * rule (MOIRA abstract; Quest as named in the HiSparse abstract).
+ *
+ * mode ASP_SUMMARIZE_BULK (0): for every request b and logical page p < N_b,
+ *   recompute summaries[block_table[b,p], h] from the page's valid tokens
+ *   (positions < T_b). k_new / v_new must be NULL.
+ * mode ASP_SUMMARIZE_APPEND (1): seq_lens already count one new token per
+ *   request (T_b >= 1). Writes k_new[b,h,:] / v_new[b,h,:] (bf16 [B, Hkv, d])
+ *   into slot (T_b-1) % P of page (T_b-1) / P of k_cache / v_cache, and folds
+ *   the new key into that page's summary (a fresh page, slot 0, takes the key
+ *   as both its min and max). Idempotent, so replaying it is safe.
+ * Requests with T_b == 0 are skipped. Out-of-range table entries set
+ * ASP_DEVERR_PAGE_RANGE and skip the page.
+ */
+#define ASP_SUMMARIZE_BULK 0
+#define ASP_SUMMARIZE_APPEND 1
+asp_status asp_page_summarize(const asp_paged_kv* kv, int32_t mode,
+                              const uint16_t* k_new, const uint16_t* v_new,
+                              void* ws, size_t ws_bytes, asp_stream stream);
+
+/*
+ * Coverage selection (MOIRA abstract: a coverage rule keeps the smallest set
+ * of pages whose estimated attention mass reaches gamma, per request, layer,
+ * KV head and step).
+ *
+ * For each segment (b, kv head h), with g query heads q[b, h*g .. h*g+g-1]:
+ *   score  s[p] = (1/sqrt(d)) * max over the group of
+ *                 sum_i max(q_i * min_pi, q_i * max_pi)        (fp32)
+ *   mass   softmax of s over the N_b pages
+ *   rank   score descending, ties to the lower logical page id
+ *   keep   the smallest prefix of the ranking whose mass reaches gamma
+ *          (gamma >= 1 keeps all N_b pages); budget > 0 instead keeps the
+ *          top min(budget, N_b) pages (fixed-budget comparison mode).
+ * q      : fp32 [B, Hq, d].
+ * gamma  : in (0, 1]; ignored when budget > 0.
+ * lists  : int32 [B, Hkv, max_pages] out; row (b,h) receives the kept logical
+ *          page ids in ascending order; entries past lens[b,h] are untouched.
+ * lens   : int32 [B, Hkv] out; the kept count (0 only when T_b == 0).
+ * Masses are summed in 64-bit fixed point, so the result is deterministic.
+ */
+asp_status asp_coverage_select(const asp_paged_kv* kv, const float* q, float gamma,
+                               int32_t budget, int32_t* lists, int32_t* lens,
+                               void* ws, size_t ws_bytes, asp_stream stream);
+
+/*
+ * Self-planning sparse attention (MOIRA abstract: each thread block derives
+ * its own share of the work from the list lengths, so the step stays inside
+ * the CUDA graph).
+ *
+ * For each query head h of segment (b, h/g), exact softmax attention over the
+ * valid tokens of the listed pages:
+ *   out[b,h,:] = sum_t softmax_t(sm_scale * q[b,h].k_t) v_t
+ *   lse[b,h]   = log sum_t exp(sm_scale * q[b,h].k_t)
+ * The grid is a fixed number of CTAs; each loads the lengths, splits the
+ * concatenated lists evenly, attends over its slice and merges partial
+ * results by log-sum-exp. A segment with lens 0 gets out = 0, lse = -inf.
+ * K/V are bf16; the products run on tensor cores with fp32 accumulation and
+ * the probabilities are rounded to bf16 for the P.V product.
+ * lists, lens : as written by asp_coverage_select (any order within a list).
+ * out : fp32 [B, Hq, d]; lse : fp32 [B, Hq] (natural log).
+ */
+asp_status asp_sparse_decode(const asp_paged_kv* kv, const float* q,
+                             const int32_t* lists, const int32_t* lens, float sm_scale,
+                             float* out, float* lse,
+                             void* ws, size_t ws_bytes, asp_stream stream);
+
+/*
+ * Synchronises `stream`, copies the device error word into *code_out
+ * (0 = none; else a mask of ASP_DEVERR_* bits), clears it and returns
+ * ASP_EDEVICE if it was non-zero, else ASP_OK. After an error, call
+ * asp_workspace_init before reusing the workspace. Not capturable.
+ */
+asp_status asp_get_device_error(void* ws, uint32_t* code_out, asp_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ASP_H_ */
