@@ -13,13 +13,16 @@
 // CTA to finish a segment; it merges the partials by log-sum-exp and resets
 // the counter, so nothing ever waits on another CTA.
 //
-// Data path (per CTA: 8 consumer warps + 1 producer warp, one CTA per SM):
-// the producer resolves list entry -> logical page -> physical page and
-// issues 2-D TMA loads of the page's K and V in 16-token sub-tiles ([16 rows x
-// 64 channels], 128-byte swizzle) into a shared-memory ring tracked by
-// mbarriers. Consumer warp w takes stages w, w+8, ... of the current piece and
-// keeps its own online-softmax state; the warps are merged in shared memory
-// at the end of each piece.
+// Data path (per CTA: 8 warps, one CTA per SM): every warp runs its own
+// pipeline. Warp w takes stages w, w+8, ... of the CTA's slice (a stage is a
+// 16-token sub-tile of one page: K then V, [16 rows x 64 channels] 2-D TMA
+// boxes with the 128-byte swizzle), keeps kSlots of them in flight in its own
+// shared-memory slots, each with its own mbarrier, and refills a slot as soon
+// as it has consumed it. Its lanes resolve list entry -> logical page ->
+// physical row for the next 32 stages ahead of time. Independent issuers per
+// SM are what reach the copy bandwidth on this gather; one issuing thread per
+// CTA does not. Each warp keeps its own online-softmax state; the warps are
+// merged in shared memory at the end of each piece.
 //
 // Per page the contraction is small (g <= 8 queries against P tokens), so it
 // runs on mma.sync m16n8k16 bf16 with tokens as the M dimension and the query
@@ -34,6 +37,8 @@
 
 #include <cudaTypedefs.h>
 
+#include <climits>
+
 #include <mutex>
 
 namespace asp {
@@ -41,15 +46,10 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kDecWarps = 8;
-constexpr int kDecThreads = (kDecWarps + 1) * 32;
-constexpr int kRingBudget = 131072;  // bytes of the K/V ring
+constexpr int kDecThreads = kDecWarps * 32;
 
-// The ring is staged in 16-token sub-tiles of a page (P/16 stages per page),
-// so a stage is 8 KiB (d=128) or 4 KiB (d=64) for every page size. Stage `it`
-// goes to ring slot it % kStages and to consumer warp it % 8; with kStages a
-// multiple of 8 every slot belongs to one warp, which has consumed the slot's
-// previous use itself before it waits on the slot again. That keeps each
-// mbarrier at most one phase from its waiter, which parity waits require.
+// A stage is a 16-token sub-tile of a page (P/16 stages per page): 8 KiB (d=128)
+// or 4 KiB (d=64). Each warp owns kSlots stages of the 128 KiB ring.
 template <int D, int P>
 struct Cfg {
   static constexpr int kHalves = D / 64;
@@ -57,8 +57,8 @@ struct Cfg {
   static constexpr int kTileBytes = 16 * 128;               // [16 rows x 64 bf16], swizzled
   static constexpr int kPartBytes = kHalves * kTileBytes;   // K (or V) of 16 tokens
   static constexpr int kStageBytes = 2 * kPartBytes;        // K then V
-  static constexpr int kStages = kRingBudget / kStageBytes; // 16 (d=128) or 32 (d=64)
-  static_assert(kStages % kDecWarps == 0, "ring slots must be owned by single warps");
+  static constexpr int kSlots = D == 128 ? 2 : 4;           // stages in flight per warp
+  static constexpr int kRingBytes = kDecWarps * kSlots * kStageBytes;
   static constexpr int kMergeFloats = kDecWarps * (2 * 8 + 8 * D);
   static constexpr int kSlotFloats = 2 * 8 + 8 * D;
 };
@@ -137,23 +137,19 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* ring = smem;
-  float* merge = reinterpret_cast<float*>(ring + C::kStages * C::kStageBytes);
-  int4* meta = reinterpret_cast<int4*>(merge + C::kMergeFloats);
-  uint64_t* full = reinterpret_cast<uint64_t*>(meta + C::kStages);
-  uint64_t* empty = full + C::kStages;
-  int* flags = reinterpret_cast<int*>(empty + C::kStages);  // [0] last-arriver, [1] warp sums...
-  int* prefix = flags + 48;                                  // [S + 1]
+  uint8_t* ring = smem;                                                  // [warp][slot][stage]
+  float* merge = reinterpret_cast<float*>(ring + C::kRingBytes);
+  int4* meta = reinterpret_cast<int4*>(merge + C::kMergeFloats);         // [warp][slot]
+  uint64_t* full = reinterpret_cast<uint64_t*>(meta + kDecWarps * C::kSlots);
+  int* flags = reinterpret_cast<int*>(full + kDecWarps * C::kSlots);    // [0..2] merge, [8..] scan
+  int* prefix = flags + 48;                                              // [S + 1]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.B * p.Hkv;
   const int G = gridDim.x, cta = blockIdx.x;
 
   if (tid == 0) {
-    for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
-    }
+    for (int i = 0; i < kDecWarps * C::kSlots; ++i) mbar_init(&full[i], 1);
     mbar_fence_init();
     prefix[0] = 0;
   }
@@ -193,102 +189,117 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     beg = (long long)cta * total / geff;
     end = (long long)(cta + 1) * total / geff;
   }
-
-  if (warp == kDecWarps) {
-    // =============================================================== producer
-    if (beg >= end) return;
-    if (lane == 0) {
-      prefetch_tensormap(&tmK);
-      prefetch_tensormap(&tmV);
-    }
-    bool aborted = false;
-    int issued = 0;
-    for (long long base = beg; base < end && !aborted; base += 32) {
-      const long long pos = base + lane;
-      int ok = 0, row = 0, ntok = 0, lp = -1;
-      if (pos < end) {
-        const int s = seg_of(prefix, S, (int)pos);
-        const int b = s / p.Hkv, h = s % p.Hkv;
-        const int T = clamp_seq_len(p.seq_lens[b], p.max_pages, P, nullptr);
-        const int n_b = ceil_div(T, P);
-        lp = __ldg(p.lists + (size_t)s * p.max_pages + (int)(pos - prefix[s]));
-        if (lp < 0 || lp >= n_b) {
-          report(p.err, ASP_DEVERR_LIST_RANGE);
-        } else {
-          const int phys = __ldg(p.bt + (size_t)b * p.max_pages + lp);
-          if (phys < 0 || phys >= p.num_phys) {
-            report(p.err, ASP_DEVERR_PAGE_RANGE);
-          } else {
-            ok = 1;
-            row = (phys * p.Hkv + h) * P;
-            ntok = min(P, T - lp * P);
-          }
-        }
-      }
-      const int nb = (int)min(32LL, end - base);
-      for (int i = 0; i < nb && !aborted; ++i) {
-        const int r_ok = __shfl_sync(kFull, ok, i);
-        const int r_row = __shfl_sync(kFull, row, i);
-        const int r_ntok = __shfl_sync(kFull, ntok, i);
-        const int r_lp = __shfl_sync(kFull, lp, i);
-#pragma unroll 1
-        for (int sub = 0; sub < C::kSubs; ++sub) {
-          // stage `it` = 16-token sub-tile `sub` of the page at position base + i
-          const int it = (int)(base + i - beg) * C::kSubs + sub;
-          const int stage = it % C::kStages;
-          const int sub_ntok = min(16, max(0, r_ntok - 16 * sub));
-          if (lane == 0) {
-            if (!mbar_wait(&empty[stage], ((it / C::kStages) & 1) ^ 1)) {
-              report(p.err, ASP_DEVERR_TIMEOUT);
-              aborted = true;
-            } else {
-              const bool load = r_ok && sub_ntok > 0;
-              meta[stage] = make_int4(r_lp, sub_ntok, load ? 1 : 0, 0);
-              uint8_t* dst = ring + stage * C::kStageBytes;
-              if (load) {
-                mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-#pragma unroll
-                for (int hh = 0; hh < C::kHalves; ++hh) {
-                  tma_load_2d(dst + hh * C::kTileBytes, &tmK, hh * 64, r_row + 16 * sub,
-                              &full[stage]);
-                  tma_load_2d(dst + C::kPartBytes + hh * C::kTileBytes, &tmV, hh * 64,
-                              r_row + 16 * sub, &full[stage]);
-                }
-              } else {
-                mbar_arrive(&full[stage]);
-              }
-              ++issued;
-            }
-          }
-          aborted = __shfl_sync(kFull, aborted ? 1 : 0, 0) != 0;
-          if (aborted) break;
-        }
-      }
-    }
-    issued = __shfl_sync(kFull, issued, 0);
-    if (lane == 0)  // never leave the CTA with copies in flight
-      for (int it = max(0, issued - C::kStages); it < issued; ++it)
-        mbar_wait(&full[it % C::kStages], (it / C::kStages) & 1);
-    return;
-  }
-
-  // ================================================================ consumers
-  const int ctid = tid;  // 0..255
-  const int gid = lane >> 2, tq = lane & 3;
   const float kLn2 = 0.69314718055994530942f;
 
   // segments with an empty list: out = 0, lse = -inf
   for (int s = cta; s < S; s += G) {
     if (prefix[s + 1] != prefix[s]) continue;
     const int b = s / p.Hkv, h = s % p.Hkv;
-    for (int e = ctid; e < p.g * D; e += kDecWarps * 32)
+    for (int e = tid; e < p.g * D; e += kDecThreads)
       p.out[((size_t)b * p.Hq + h * p.g + e / D) * D + e % D] = 0.f;
-    for (int e = ctid; e < p.g; e += kDecWarps * 32)
-      p.lse[(size_t)b * p.Hq + h * p.g + e] = -INFINITY;
+    for (int e = tid; e < p.g; e += kDecThreads) p.lse[(size_t)b * p.Hq + h * p.g + e] = -INFINITY;
   }
   if (beg >= end) return;
+  if (tid == 0) {
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
 
+  // ---- this warp's stages: CTA stage it = warp + 8n covers page position
+  // beg + it / kSubs, sub-tile it % kSubs (= warp % kSubs, since kSubs | 8)
+  const long long nst = (end - beg) * C::kSubs;
+  const int n_total = nst > warp ? (int)((nst - warp + kDecWarps - 1) / kDecWarps) : 0;
+  const int sub = warp % C::kSubs;
+  uint8_t* my_ring = ring + warp * C::kSlots * C::kStageBytes;
+  uint64_t* my_full = full + warp * C::kSlots;
+  int4* my_meta = meta + warp * C::kSlots;
+
+  // Lookups for warp stages [nb, nb + 32): lane j owns stage nb + j. The
+  // list entry (and sequence length) are fetched two batches ahead and the
+  // block-table entry one batch ahead of the stages being issued.
+  constexpr int kNoPage = INT_MIN;
+  auto lookup_list = [&](int nb, int& seg, int& T, int& lp) {
+    seg = 0; T = 0; lp = -1;
+    const int n = nb + lane;
+    if (n < n_total) {
+      const long long pos = beg + (warp + (long long)kDecWarps * n) / C::kSubs;
+      seg = seg_of(prefix, S, (int)pos);
+      T = __ldg(p.seq_lens + seg / p.Hkv);
+      lp = __ldg(p.lists + (size_t)seg * p.max_pages + (int)(pos - prefix[seg]));
+    }
+  };
+  auto lookup_page = [&](int nb, int seg, int T, int lp) {
+    int phys = kNoPage;
+    if (nb + lane < n_total) {
+      T = min(max(T, 0), p.max_pages * P);
+      if (lp < 0 || lp >= ceil_div(T, P)) {
+        if (sub == 0) report(p.err, ASP_DEVERR_LIST_RANGE);
+      } else {
+        phys = __ldg(p.bt + (size_t)(seg / p.Hkv) * p.max_pages + lp);
+      }
+    }
+    return phys;
+  };
+  // (row of the sub-tile in the [rows, d] view, valid tokens in it) or ntok 0
+  auto finalize = [&](int seg, int T, int lp, int phys, int& row, int& ntok) {
+    row = 0; ntok = 0;
+    if (phys == kNoPage) return;
+    if (phys < 0 || phys >= p.num_phys) {
+      if (sub == 0) report(p.err, ASP_DEVERR_PAGE_RANGE);
+      return;
+    }
+    T = min(max(T, 0), p.max_pages * P);
+    row = (phys * p.Hkv + seg % p.Hkv) * P + 16 * sub;
+    ntok = min(16, max(0, min(P, T - lp * P) - 16 * sub));
+  };
+
+  int sB, TB, lpB, sC, TC, lpC, rowA, ntokA, phB;
+  {
+    int sA, TA, lpA;
+    lookup_list(0, sA, TA, lpA);
+    lookup_list(32, sB, TB, lpB);
+    const int phA = lookup_page(0, sA, TA, lpA);
+    finalize(sA, TA, lpA, phA, rowA, ntokA);
+    phB = lookup_page(32, sB, TB, lpB);
+    lookup_list(64, sC, TC, lpC);
+  }
+  int ib = 0;   // first warp stage of batch A
+  int ni = 0;   // next warp stage to issue
   bool aborted = false;
+  auto issue_next = [&]() {
+    if (ni >= ib + 32) {  // rotate the lookup batches (warp-uniform)
+      finalize(sB, TB, lpB, phB, rowA, ntokA);
+      ib += 32;
+      const int phC = lookup_page(ib + 32, sC, TC, lpC);
+      sB = sC; TB = TC; lpB = lpC; phB = phC;
+      lookup_list(ib + 64, sC, TC, lpC);
+    }
+    const int r_row = __shfl_sync(kFull, rowA, ni - ib);
+    const int r_ntok = __shfl_sync(kFull, ntokA, ni - ib);
+    if (lane == 0) {
+      const int slot = ni % C::kSlots;
+      my_meta[slot] = make_int4(r_ntok, 0, 0, 0);
+      if (r_ntok > 0) {
+        uint8_t* dst = my_ring + slot * C::kStageBytes;
+        mbar_arrive_expect_tx(&my_full[slot], C::kStageBytes);
+#pragma unroll
+        for (int hh = 0; hh < C::kHalves; ++hh) {
+          tma_load_2d(dst + hh * C::kTileBytes, &tmK, hh * 64, r_row, &my_full[slot]);
+          tma_load_2d(dst + C::kPartBytes + hh * C::kTileBytes, &tmV, hh * 64, r_row,
+                      &my_full[slot]);
+        }
+      } else {
+        mbar_arrive(&my_full[slot]);
+      }
+    }
+    ++ni;
+  };
+  while (ni < min(C::kSlots, n_total)) issue_next();
+
+  // ================================================================ pieces
+  const int gid = lane >> 2, tq = lane & 3;
+  int nc = 0;      // next warp stage to consume
+  int waited = 0;  // stages whose copies are known complete
   long long pos = beg;
   while (pos < end) {
     const int s = seg_of(prefix, S, (int)pos);
@@ -320,31 +331,39 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 #pragma unroll
     for (int dt = 0; dt < D / 16; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
 
-    const int it0 = (int)(pos - beg) * C::kSubs, it1 = (int)(pe - beg) * C::kSubs;
-    for (int it = it0 + ((warp - it0) % kDecWarps + kDecWarps) % kDecWarps; it < it1;
-         it += kDecWarps) {
-      const int stage = it % C::kStages;
-      if (!aborted && !mbar_wait(&full[stage], (it / C::kStages) & 1)) {
-        if (lane == 0) report(p.err, ASP_DEVERR_TIMEOUT);
-        aborted = true;
+    const long long it_end = (pe - beg) * C::kSubs;
+    while (nc < n_total && warp + (long long)kDecWarps * nc < it_end) {
+      const int slot = nc % C::kSlots;
+      if (!aborted) {
+        // warp-uniform outcome: the refill below shuffles across all lanes
+        const bool got = mbar_wait(&my_full[slot], (nc / C::kSlots) & 1);
+        if (__all_sync(kFull, got)) {
+          waited = nc + 1;
+        } else {
+          if (lane == 0) report(p.err, ASP_DEVERR_TIMEOUT);
+          aborted = true;
+        }
       }
-      const int4 mt = meta[stage];
-      if (!aborted && mt.z) {
-        const int ntok = mt.y;
-        const uint32_t kb = smem_u32(ring + stage * C::kStageBytes);
+      const int ntok = my_meta[slot].x;
+      if (!aborted && ntok > 0) {
+        const uint32_t kb = smem_u32(my_ring + slot * C::kStageBytes);
         const uint32_t vb = kb + C::kPartBytes;
         const int j = lane >> 3;
         // ---- S^T[16 x 8] = K[16 x d] . Q^T[d x 8]
-        float sv[4] = {0.f, 0.f, 0.f, 0.f};
+        float sv[4];
         {
+          // four independent accumulator chains (hi/lo x even/odd k-step)
+          float acc[4][4] = {};
           const int r = (j & 1) * 8 + (lane & 7);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             uint32_t a[4];
             ldsm_x4(kb + swz(r, kk * 16 + (j >> 1) * 8), a);
-            mma16816(sv, a, qhi[kk][0], qhi[kk][1]);
-            mma16816(sv, a, qlo[kk][0], qlo[kk][1]);
+            mma16816(acc[(kk & 1) * 2], a, qhi[kk][0], qhi[kk][1]);
+            mma16816(acc[(kk & 1) * 2 + 1], a, qlo[kk][0], qlo[kk][1]);
           }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sv[i] = (acc[0][i] + acc[2][i]) + (acc[1][i] + acc[3][i]);
         }
         // ---- mask tokens past the sequence, online softmax (log2 domain)
         if (gid >= ntok) sv[0] = sv[1] = -INFINITY;
@@ -374,7 +393,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const uint32_t pb1 = movm_t(pack_bf16(p2, p3));
         // ---- rows past the sequence may hold anything: zero them in V
         if (ntok < 16) {
-          uint8_t* vpart = ring + stage * C::kStageBytes + C::kPartBytes;
+          uint8_t* vpart = my_ring + slot * C::kStageBytes + C::kPartBytes;
           const int chunks = (16 - ntok) * C::kHalves * 8;
           for (int e = lane; e < chunks; e += 32) {
             const int r = ntok + e / (C::kHalves * 8);
@@ -382,7 +401,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             *reinterpret_cast<uint4*>(vpart + hh * C::kTileBytes + r * 128 + (e % 8) * 16) =
                 make_uint4(0, 0, 0, 0);
           }
-          fence_proxy_async_smem();
           __syncwarp();
         }
         // ---- O^T[d x 8] += V^T[d x 16] . P^T[16 x 8]
@@ -396,8 +414,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           }
         }
       }
+      // the slot's reads (and any zeroing writes) are done: refill it
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
+      if (!aborted && ni < n_total) {
+        fence_proxy_async_smem();
+        issue_next();
+      }
+      ++nc;
     }
 
     // ---- merge the 8 warps' states of this piece
@@ -421,10 +444,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       mw[16 + (2 * tq) * D + d0 + 8] = o[dt][2];
       mw[16 + (2 * tq + 1) * D + d0 + 8] = o[dt][3];
     }
-    named_bar_sync(1, kDecWarps * 32);
+    __syncthreads();
     const bool whole = (pos == seg_lo) && (pe == seg_hi);
-    float* slot = p.partials + (size_t)(s + cta) * p.slot_floats;
-    for (int e = ctid; e < p.g * D; e += kDecWarps * 32) {
+    float* pslot = p.partials + (size_t)(s + cta) * p.slot_floats;
+    for (int e = tid; e < p.g * D; e += kDecThreads) {
       const int col = e / D, d = e % D;
       float M = -INFINITY;
 #pragma unroll
@@ -444,17 +467,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         p.out[row * D + d] = L > 0.f ? acc / L : 0.f;
         if (d == 0) p.lse[row] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
       } else {
-        slot[16 + col * D + d] = acc;
+        pslot[16 + col * D + d] = acc;
         if (d == 0) {
-          slot[col] = M;
-          slot[8 + col] = L;
+          pslot[col] = M;
+          pslot[8 + col] = L;
         }
       }
     }
     if (!whole) {
       __threadfence();
-      named_bar_sync(1, kDecWarps * 32);
-      if (ctid == 0) {
+      __syncthreads();
+      if (tid == 0) {
         const int cf = cta_of(seg_lo, total, geff), cl = cta_of(seg_hi - 1, total, geff);
         const int prev = atomicAdd(&p.counters[s], 1);
         const int last = prev == cl - cf;
@@ -463,11 +486,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         flags[1] = cf;
         flags[2] = cl;
       }
-      named_bar_sync(1, kDecWarps * 32);
+      __syncthreads();
       if (flags[0]) {
         __threadfence();
         const int cf = flags[1], cl = flags[2];
-        for (int e = ctid; e < p.g * D; e += kDecWarps * 32) {
+        for (int e = tid; e < p.g * D; e += kDecThreads) {
           const int col = e / D, d = e % D;
           float M = -INFINITY;
           for (int c = cf; c <= cl; ++c)
@@ -487,9 +510,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
       }
     }
-    named_bar_sync(1, kDecWarps * 32);  // merge area is rewritten by the next piece
+    __syncthreads();  // the merge area is rewritten by the next piece
     pos = pe;
   }
+  // never leave the CTA with copies in flight (only after a timeout can any remain)
+  if (lane == 0)
+    for (int n = waited; n < ni; ++n) mbar_wait(&my_full[n % C::kSlots], (n / C::kSlots) & 1);
 }
 
 // ----------------------------------------------------------------- host side
@@ -526,8 +552,8 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
   using C = Cfg<D, P>;
   const asp_paged_kv& kv = *a.kv;
   const int S = kv.batch * kv.num_kv_heads;
-  const size_t smem = 1024 + (size_t)C::kStages * C::kStageBytes + C::kMergeFloats * 4 +
-                      C::kStages * sizeof(int4) + 2 * C::kStages * 8 + 48 * 4 + (S + 1) * 4;
+  const size_t smem = 1024 + (size_t)C::kRingBytes + C::kMergeFloats * 4 +
+                      kDecWarps * C::kSlots * (sizeof(int4) + 8) + 48 * 4 + (S + 1) * 4;
   cudaError_t e = set_max_dynamic_smem((const void*)decode_kernel<D, P>, (int)smem);
   if (e != cudaSuccess) return e;
   const long long rows = (long long)kv.num_phys_pages * kv.num_kv_heads * P;

@@ -2,28 +2,32 @@
 // head and step, keep the smallest page set whose estimated attention mass
 // reaches gamma). Two kernels:
 //
-// score_kernel   HBM-bound stream over the page summaries. Persistent CTAs
-//                split the concatenated (request, page) space evenly. One
-//                producer warp stages each physical page's summaries (all KV
-//                heads, contiguous) into a shared-memory ring with 1-D bulk
-//                copies; eight consumer warps each own one (page slot, KV
-//                head) of a stage. A lane holds 8 (d=128) or 4 (d=64)
-//                channels of either the min row or the max row, together with
-//                the matching sign part of the group's queries, so
+// score_kernel   HBM-bound stream over the page summaries. A CTA takes 32
+//                logical pages of one request; warp w owns KV head w % Hkv and
+//                reads its 4d-byte (page, head) unit with one coalesced warp
+//                load (16 bytes per lane), 8 pages in flight. A lane holds 8
+//                (d=128) or 4 (d=64) channels of either the min row or the
+//                max row, together with the matching sign part of the group's
+//                queries, so
 //                sum_i max(q_i*mn_i, q_i*mx_i) = sum_i q-_i*mn_i + q+_i*mx_i
 //                is one fp32 FMA per element (paired with fma.rn.f32x2). A
 //                transpose-reduce leaves each head's sum on a lane group; the
 //                group max times 1/sqrt(d) is the page score. Scores stay
 //                fp32: bf16 queries would move them by ~1e-3 and change lists.
+//                (Plain 16-byte loads from many warps reach the copy
+//                bandwidth on this gather; a single-thread bulk-copy ring per
+//                CTA does not.)
 //
 // select_kernel  One CTA per segment. Softmax weights exp(s - max) are turned
-//                into 64-bit fixed point (2^40 = weight of the top page), so
-//                every sum is exact and order-independent. A radix select over
+//                into fixed point (2^38 = weight of the top page), so every
+//                sum is exact and order-independent. A radix select over
 //                order-preserving score keys, with histograms of count and
 //                mass over the candidates' actual key range, finds the cutoff
 //                score in at most four rounds; ties at the cutoff go to the
 //                lower page ids; one block scan compacts the kept ids in
-//                ascending order.
+//                ascending order. Each warp fills a private histogram of
+//                32-bit words (a mass is three 13-bit limbs, so no word can
+//                overflow), which keeps hot bins from serialising the CTA.
 #include "asp_internal.cuh"
 
 namespace asp {
@@ -32,9 +36,9 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 
 // ============================================================== score kernel
-constexpr int kScoreConsumerWarps = 8;
-constexpr int kScoreThreads = (kScoreConsumerWarps + 1) * 32;
-constexpr int kScoreStages = 16;
+constexpr int kScoreWarps = 8;
+constexpr int kScoreThreads = kScoreWarps * 32;
+constexpr int kScoreChunk = 32;  // logical pages per CTA
 
 struct ScoreParams {
   const uint16_t* summ;
@@ -47,19 +51,24 @@ struct ScoreParams {
   float inv_sqrt_d;
 };
 
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  uint64_t ra, rb, rc, rd;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
-  float2 d;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 unpack2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
 }
-
-__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
-  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+// bf16x2 word -> (low element, high element) as an fp32 pair
+__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
+  return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
 // Sum of v[j] over the 32 lanes for each j < G, then the max over j. The
@@ -84,176 +93,95 @@ __device__ __forceinline__ float group_bound_max(float (&v)[G], int lane) {
   return s;
 }
 
-// Segment of the concatenated page space holding position pos: the largest
-// r with prefix[r] <= pos (prefix non-decreasing, prefix[0] = 0, pos < prefix[n]).
-__device__ __forceinline__ int find_owner(const int* prefix, int n, int pos) {
-  int lo = 0, hi = n - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (prefix[mid] <= pos) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
+// Lane slice of one (page, head) summary unit (min row then max row, 4d bytes):
+// 16 bytes (d=128) or 8 bytes (d=64).
+template <int D>
+struct UnitVec;
+template <>
+struct UnitVec<128> {
+  using T = uint4;
+};
+template <>
+struct UnitVec<64> {
+  using T = uint2;
+};
 
+// CTA (x, y) = pages [32x, 32x+32) of request y. Warp w owns KV head w % Hkv and
+// every (8/Hkv)-th page of the chunk; one warp load of 32 lanes covers one
+// (page, head) unit exactly, and 4-8 pages are in flight per warp.
 template <int D, int G>
 __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(ScoreParams p) {
-  constexpr int kUnitBytes = 4 * D;            // min row + max row, bf16
-  constexpr int kStageBytes = 8 * kUnitBytes;  // 8 (page, head) units
-  constexpr int kCpl = D / 16;                 // channels per lane
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* ring = smem;
-  int2* meta = reinterpret_cast<int2*>(ring + kScoreStages * kStageBytes);  // [stage][8 slots]
-  uint64_t* full = reinterpret_cast<uint64_t*>(meta + kScoreStages * 8);
-  uint64_t* empty = full + kScoreStages;
-  int* req_prefix = reinterpret_cast<int*>(empty + kScoreStages);  // [B + 1]
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int pps = 8 / p.Hkv;  // pages per stage
-  if (tid == 0) {
-    for (int i = 0; i < kScoreStages; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kScoreConsumerWarps);
-    }
-    mbar_fence_init();
-  }
-  // request prefix of page counts (clamped sequence lengths)
-  if (warp == 0) {
-    int carry = 0;
-    if (lane == 0) req_prefix[0] = 0;
-    for (int b0 = 0; b0 < p.B; b0 += 32) {
-      const int b = b0 + lane;
-      int n = 0;
-      if (b < p.B) n = ceil_div(clamp_seq_len(p.seq_lens[b], p.max_pages, p.P, p.err), p.P);
-      int x = n;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(kFull, x, o);
-        if (lane >= o) x += y;
-      }
-      if (b < p.B) req_prefix[b + 1] = carry + x;
-      carry += __shfl_sync(kFull, x, 31);
-    }
-  }
-  __syncthreads();
-  const int total = req_prefix[p.B];
-  const int beg = (int)((long long)blockIdx.x * total / gridDim.x);
-  const int end = (int)((long long)(blockIdx.x + 1) * total / gridDim.x);
-  const int nstages = ceil_div(end - beg, pps);
-
-  if (warp == kScoreConsumerWarps) {
-    // ------------------------------------------------------------ producer
-    bool aborted = false;
-    int issued = 0;
-    for (int base = beg; base < end && !aborted; base += 32) {
-      const int pos = base + lane;
-      int b = -1, lp = -1, phys = -1;
-      if (pos < end) {
-        b = find_owner(req_prefix, p.B + 1, pos);
-        lp = pos - req_prefix[b];
-        phys = __ldg(p.bt + (size_t)b * p.max_pages + lp);
-        if (phys < 0 || phys >= p.num_phys) {
-          report(p.err, ASP_DEVERR_PAGE_RANGE);
-          phys = -1;
-        }
-      }
-      for (int j = 0; j < 32 && base + j < end; j += pps) {
-        const int it = (base + j - beg) / pps;
-        const int stage = it % kScoreStages;
-        if (lane == 0 && !mbar_wait(&empty[stage], ((it / kScoreStages) & 1) ^ 1)) {
-          report(p.err, ASP_DEVERR_TIMEOUT);
-          aborted = true;
-        }
-        aborted = __shfl_sync(kFull, aborted ? 1 : 0, 0) != 0;
-        if (aborted) break;
-        uint32_t bytes = 0;
-        for (int u = 0; u < pps; ++u) {
-          const int src = j + u;
-          const int ub = __shfl_sync(kFull, b, src & 31);
-          const int ulp = __shfl_sync(kFull, lp, src & 31);
-          const int uph = __shfl_sync(kFull, phys, src & 31);
-          const bool in = (src < 32) && (base + src < end) && uph >= 0;
-          if (lane == 0) meta[stage * 8 + u] = in ? make_int2(ub, ulp) : make_int2(-1, -1);
-          if (in) bytes += p.Hkv * kUnitBytes;
-        }
-        if (lane == 0) {
-          if (bytes) {
-            mbar_arrive_expect_tx(&full[stage], bytes);
-          } else {
-            mbar_arrive(&full[stage]);
-          }
-        }
-        for (int u = 0; u < pps; ++u) {
-          const int src = j + u;
-          const int uph = __shfl_sync(kFull, phys, src & 31);
-          const bool in = (src < 32) && (base + src < end) && uph >= 0;
-          if (lane == 0 && in)
-            bulk_g2s(ring + stage * kStageBytes + u * p.Hkv * kUnitBytes,
-                     p.summ + (size_t)uph * p.Hkv * 2 * D, p.Hkv * kUnitBytes, &full[stage]);
-        }
-        ++issued;
-      }
-    }
-    // never leave the CTA with copies in flight
-    if (lane == 0)
-      for (int it = max(0, issued - kScoreStages); it < issued; ++it)
-        mbar_wait(&full[it % kScoreStages], (it / kScoreStages) & 1);
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers
-  const int slot = warp / p.Hkv, head = warp % p.Hkv;
+  using V = typename UnitVec<D>::T;
+  constexpr int kCpl = D / 16;                             // channels per lane
+  constexpr int kScoreUnroll = (G * kCpl >= 64) ? 4 : 8;   // pages in flight per warp
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int b = blockIdx.y;
+  const int N = ceil_div(clamp_seq_len(p.seq_lens[b], p.max_pages, p.P, p.err), p.P);
+  const int c0 = blockIdx.x * kScoreChunk;
+  if (c0 >= N) return;
+  const int head = warp % p.Hkv, wph = kScoreWarps / p.Hkv, sub = warp / p.Hkv;
   const int part = lane >> 4;  // 0: min row, paired with q-; 1: max row, paired with q+
-  const int c0 = (lane & 15) * kCpl;
-  float qv[G][kCpl];
-  int cur_b = -1;
-  bool aborted = false;
-  for (int it = 0; it < nstages; ++it) {
-    const int stage = it % kScoreStages;
-    if (!aborted && !mbar_wait(&full[stage], (it / kScoreStages) & 1)) {
-      if (lane == 0) report(p.err, ASP_DEVERR_TIMEOUT);
-      aborted = true;
+  const int cl = (lane & 15) * kCpl;
+
+  // the group's queries, sign part matching this lane's row, as fp32 pairs
+  uint64_t qv[G][kCpl / 2];
+  {
+    const float* qb = p.q + ((size_t)b * p.Hq + head * G) * D + cl;
+#pragma unroll
+    for (int j = 0; j < G; ++j)
+#pragma unroll
+      for (int i = 0; i < kCpl; i += 4) {
+        const float4 x = *reinterpret_cast<const float4*>(qb + (size_t)j * D + i);
+        const float a0 = part ? fmaxf(x.x, 0.f) : fminf(x.x, 0.f);
+        const float a1 = part ? fmaxf(x.y, 0.f) : fminf(x.y, 0.f);
+        const float a2 = part ? fmaxf(x.z, 0.f) : fminf(x.z, 0.f);
+        const float a3 = part ? fmaxf(x.w, 0.f) : fminf(x.w, 0.f);
+        qv[j][i / 2] = pack2(a0, a1);
+        qv[j][i / 2 + 1] = pack2(a2, a3);
+      }
+  }
+  const int npg = min(kScoreChunk, N - c0);               // pages of this chunk
+  const int mine = (npg - sub + wph - 1) / wph;           // pages of this warp
+  const int32_t* bt_row = p.bt + (size_t)b * p.max_pages + c0 + sub;
+  float* out = p.scores + ((size_t)b * p.Hkv + head) * p.max_pages + c0 + sub;
+  const int unit_off = head * 4 * D + lane * (int)sizeof(V);  // bytes inside a page block
+
+  // block-table entries of this warp's pages: lane k holds page k
+  int phys = -1;
+  if (lane < mine) phys = __ldg(bt_row + lane * wph);
+  if (lane < mine && (phys < 0 || phys >= p.num_phys)) {
+    report(p.err, ASP_DEVERR_PAGE_RANGE);
+    phys = -1;
+  }
+  for (int k0 = 0; k0 < mine; k0 += kScoreUnroll) {
+    V x[kScoreUnroll];
+#pragma unroll
+    for (int u = 0; u < kScoreUnroll; ++u) {
+      const int ph = __shfl_sync(kFull, phys, (k0 + u) & 31);
+      if (k0 + u < mine && ph >= 0)
+        x[u] = __ldg(reinterpret_cast<const V*>(
+            reinterpret_cast<const uint8_t*>(p.summ) + (size_t)ph * p.Hkv * 4 * D + unit_off));
     }
-    const int2 mt = aborted ? make_int2(-1, -1) : meta[stage * 8 + slot];
-    if (mt.x >= 0) {
-      if (mt.x != cur_b) {
-        cur_b = mt.x;
-        const float* qb = p.q + ((size_t)cur_b * p.Hq + head * G) * D + c0;
 #pragma unroll
-        for (int j = 0; j < G; ++j)
+    for (int u = 0; u < kScoreUnroll; ++u) {
+      if (k0 + u >= mine) break;  // warp-uniform
+      const int ph = __shfl_sync(kFull, phys, (k0 + u) & 31);
+      const uint32_t* w = reinterpret_cast<const uint32_t*>(&x[u]);
+      uint64_t xv[kCpl / 2];
 #pragma unroll
-          for (int i = 0; i < kCpl; i += 4) {
-            const float4 x = *reinterpret_cast<const float4*>(qb + (size_t)j * D + i);
-            qv[j][i + 0] = part ? fmaxf(x.x, 0.f) : fminf(x.x, 0.f);
-            qv[j][i + 1] = part ? fmaxf(x.y, 0.f) : fminf(x.y, 0.f);
-            qv[j][i + 2] = part ? fmaxf(x.z, 0.f) : fminf(x.z, 0.f);
-            qv[j][i + 3] = part ? fmaxf(x.w, 0.f) : fminf(x.w, 0.f);
-          }
-      }
-      const uint8_t* u = ring + stage * kStageBytes + (slot * p.Hkv + head) * kUnitBytes +
-                         part * (2 * D) + c0 * 2;
-      uint32_t w[kCpl / 2];
-      if constexpr (kCpl == 8) {
-        const uint4 x = *reinterpret_cast<const uint4*>(u);
-        w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
-      } else {
-        const uint2 x = *reinterpret_cast<const uint2*>(u);
-        w[0] = x.x; w[1] = x.y;
-      }
+      for (int m = 0; m < kCpl / 2; ++m) xv[m] = bf16x2_to_f32x2(w[m]);
       float acc[G];
 #pragma unroll
       for (int j = 0; j < G; ++j) {
-        float2 a2 = make_float2(0.f, 0.f);
+        uint64_t a2 = 0;
 #pragma unroll
-        for (int m = 0; m < kCpl / 2; ++m)
-          a2 = ffma2(make_float2(qv[j][2 * m], qv[j][2 * m + 1]), bf16x2_to_float2(w[m]), a2);
-        acc[j] = a2.x + a2.y;
+        for (int m = 0; m < kCpl / 2; ++m) a2 = ffma2(qv[j][m], xv[m], a2);
+        const float2 f = unpack2(a2);
+        acc[j] = f.x + f.y;
       }
-      const float s = group_bound_max<G>(acc, lane) * p.inv_sqrt_d;
-      if (lane == 0)
-        p.scores[((size_t)mt.x * p.Hkv + head) * p.max_pages + mt.y] = s;
+      const float sc = group_bound_max<G>(acc, lane) * p.inv_sqrt_d;
+      if (lane == 0) out[(k0 + u) * wph] = ph >= 0 ? sc : -INFINITY;
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[stage]);
   }
 }
 
@@ -261,6 +189,10 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(ScoreParams p) 
 constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelCache = 8192;  // scores cached in shared memory when N fits
+constexpr int kBins = 256;
+constexpr int kLimbBits = 13;    // mass = l0 + l1 << 13 + l2 << 26, each limb < 2^13
+constexpr size_t kSelSmem = (size_t)kSelWarps * kBins * 4 * sizeof(uint32_t) +  // private hists
+                            kSelCache * sizeof(float);                            // score cache
 
 struct SelectParams {
   const float* scores;
@@ -282,9 +214,9 @@ __device__ __forceinline__ uint32_t score_key(float s) {
 __device__ __forceinline__ float key_score(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
-// Softmax weight of a page relative to the top page, in 2^-40 units.
+// Softmax weight of a page relative to the top page, in 2^-38 units (<= 2^38).
 __device__ __forceinline__ unsigned long long mass_fixed(float s, float smax) {
-  return __float2ull_rn(expf(s - smax) * 1099511627776.0f);
+  return __float2ull_rn(expf(s - smax) * 274877906944.0f);
 }
 
 template <typename T>
@@ -313,13 +245,15 @@ __device__ __forceinline__ T block_reduce(T v, T* scratch, int op /*0 sum, 1 min
 }
 
 __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
-  __shared__ float cache[kSelCache];
-  __shared__ uint32_t h_cnt[256];
-  __shared__ unsigned long long h_mass[256];
+  extern __shared__ __align__(16) uint8_t sel_smem[];
+  uint32_t* hist = reinterpret_cast<uint32_t*>(sel_smem);  // [warp][bin][count, l0, l1, l2]
+  float* cache = reinterpret_cast<float*>(hist + kSelWarps * kBins * 4);
+  __shared__ uint32_t m_cnt[kBins];
+  __shared__ unsigned long long m_mass[kBins];
   __shared__ unsigned long long red_u64[kSelWarps];
   __shared__ float red_f[kSelWarps];
-  __shared__ uint32_t pick[4];             // bin, count above (low 32), spare
-  __shared__ unsigned long long pick_m[1];  // mass above
+  __shared__ uint32_t pick[4];
+  __shared__ unsigned long long pick_m[1];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int s = blockIdx.x;
@@ -366,23 +300,42 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
   uint32_t lo = score_key(lo_s), hi = score_key(hi_s);
   unsigned long long above_m = 0;
   uint32_t above_c = 0, cnt_eq = 0;
+  uint32_t* my_hist = hist + warp * kBins * 4;
+  constexpr uint32_t kLimbMask = (1u << kLimbBits) - 1u;
   while (true) {
     const uint32_t range = hi - lo;
     const int bits = range ? 32 - __clz(range) : 0;
     const int shift = bits > 8 ? bits - 8 : 0;
-    for (int i = tid; i < 256; i += kSelThreads) {
-      h_cnt[i] = 0;
-      h_mass[i] = 0;
-    }
+    for (int i = tid; i < kSelWarps * kBins; i += kSelThreads)
+      reinterpret_cast<uint4*>(hist)[i] = make_uint4(0, 0, 0, 0);
     __syncthreads();
     for (int i = tid; i < N; i += kSelThreads) {
       const float v = sc[i];
       const uint32_t k = score_key(v);
       if (k >= lo && k <= hi) {
-        const uint32_t bin = (k - lo) >> shift;
-        atomicAdd(&h_cnt[bin], 1u);
-        if (mass_mode) atomicAdd(&h_mass[bin], mass_fixed(v, smax));
+        uint32_t* h = my_hist + ((k - lo) >> shift) * 4;
+        atomicAdd(h, 1u);
+        if (mass_mode) {
+          const unsigned long long m = mass_fixed(v, smax);
+          atomicAdd(h + 1, (uint32_t)m & kLimbMask);
+          atomicAdd(h + 2, (uint32_t)(m >> kLimbBits) & kLimbMask);
+          atomicAdd(h + 3, (uint32_t)(m >> (2 * kLimbBits)));
+        }
       }
+    }
+    __syncthreads();
+    if (tid < kBins) {  // merge the private histograms of bin tid
+      uint32_t c = 0;
+      unsigned long long l0 = 0, l1 = 0, l2 = 0;
+      for (int w = 0; w < kSelWarps; ++w) {
+        const uint4 h = reinterpret_cast<const uint4*>(hist)[w * kBins + tid];
+        c += h.x;
+        l0 += h.y;
+        l1 += h.z;
+        l2 += h.w;
+      }
+      m_cnt[tid] = c;
+      m_mass[tid] = l0 + (l1 << kLimbBits) + (l2 << (2 * kLimbBits));
     }
     __syncthreads();
     if (warp == 0) {
@@ -392,8 +345,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
       uint32_t lc = 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        lm += h_mass[lane * 8 + i];
-        lc += h_cnt[lane * 8 + i];
+        lm += m_mass[lane * 8 + i];
+        lc += m_cnt[lane * 8 + i];
       }
       unsigned long long sm = lm;  // inclusive suffix over lanes >= lane
       uint32_t scn = lc;
@@ -406,17 +359,18 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
           scn += yc;
         }
       }
-      const bool reach = mass_mode ? (above_m + sm >= target) : ((unsigned long long)above_c + scn >= target);
+      const bool reach = mass_mode ? (above_m + sm >= target)
+                                   : ((unsigned long long)above_c + scn >= target);
       const unsigned ballot = __ballot_sync(kFull, reach);
-      const int lstar = 31 - __clz(ballot);  // ballot has lane 0 set by the invariant
+      const int lstar = ballot ? 31 - __clz(ballot) : 0;  // lane 0 reaches by the invariant
       if (lane == lstar) {
         unsigned long long run_m = above_m + (sm - lm);
         uint32_t run_c = above_c + (scn - lc);
         int j = lane * 8;
         for (int i = 7; i >= 0; --i) {
           const int bin = lane * 8 + i;
-          const unsigned long long nm = run_m + h_mass[bin];
-          const uint32_t nc = run_c + h_cnt[bin];
+          const unsigned long long nm = run_m + m_mass[bin];
+          const uint32_t nc = run_c + m_cnt[bin];
           if (mass_mode ? (nm >= target) : ((unsigned long long)nc >= target)) {
             j = bin;
             break;
@@ -426,7 +380,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
         }
         pick[0] = (uint32_t)j;
         pick[1] = run_c;
-        pick[2] = h_cnt[j];
+        pick[2] = m_cnt[j];
         pick_m[0] = run_m;
       }
     }
@@ -501,15 +455,11 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
 template <int D, int G>
 cudaError_t launch_score_t(const SelectArgs& a, cudaStream_t stream) {
   const asp_paged_kv& kv = *a.kv;
-  constexpr int kStageBytes = 8 * 4 * D;
-  const size_t smem = (size_t)kScoreStages * kStageBytes + kScoreStages * 8 * sizeof(int2) +
-                      2 * kScoreStages * sizeof(uint64_t) + (kv.batch + 1) * sizeof(int);
-  cudaError_t e = set_max_dynamic_smem((const void*)score_kernel<D, G>, (int)smem);
-  if (e != cudaSuccess) return e;
   ScoreParams p{kv.summaries, a.q, kv.block_table, kv.seq_lens, a.scores, a.err,
                 kv.batch, kv.num_q_heads, kv.num_kv_heads, kv.page_size, kv.max_pages,
                 kv.num_phys_pages, 1.0f / sqrtf((float)D)};
-  score_kernel<D, G><<<a.num_sms * 2, kScoreThreads, smem, stream>>>(p);
+  dim3 grid(ceil_div(kv.max_pages, kScoreChunk), kv.batch);
+  score_kernel<D, G><<<grid, kScoreThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -536,7 +486,9 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream) {
   }
   SelectParams p{a.scores, kv.seq_lens, a.lists, a.lens, a.err, kv.num_kv_heads, kv.page_size,
                  kv.max_pages, a.gamma, a.budget};
-  select_kernel<<<kv.batch * kv.num_kv_heads, kSelThreads, 0, stream>>>(p);
+  cudaError_t e = set_max_dynamic_smem((const void*)select_kernel, (int)kSelSmem);
+  if (e != cudaSuccess) return e;
+  select_kernel<<<kv.batch * kv.num_kv_heads, kSelThreads, kSelSmem, stream>>>(p);
   return cudaGetLastError();
 }
 
