@@ -2,12 +2,13 @@
 // head and step, keep the smallest page set whose estimated attention mass
 // reaches gamma). Two kernels:
 //
-// score_kernel   HBM-bound stream over the page summaries. A CTA takes 32
-//                logical pages of one request; warp w owns KV head w % Hkv and
-//                reads its 4d-byte (page, head) unit with one coalesced warp
-//                load (16 bytes per lane), 8 pages in flight. A lane holds 8
-//                (d=128) or 4 (d=64) channels of either the min row or the
-//                max row, together with the matching sign part of the group's
+// score_kernel   HBM-bound stream over the page summaries. A CTA takes 64
+//                logical pages of one request; warp w owns KV head w % Hkv.
+//                16 lanes (32 when the group's queries would not fit in
+//                registers) cover one (page, head) unit with coalesced
+//                16-byte loads, several pages in flight per warp. A lane
+//                holds channels of either the min row or the max row,
+//                together with the matching sign part of the group's
 //                queries, so
 //                sum_i max(q_i*mn_i, q_i*mx_i) = sum_i q-_i*mn_i + q+_i*mx_i
 //                is one fp32 FMA per element (paired with fma.rn.f32x2). A
@@ -38,7 +39,7 @@ constexpr unsigned kFull = 0xffffffffu;
 // ============================================================== score kernel
 constexpr int kScoreWarps = 8;
 constexpr int kScoreThreads = kScoreWarps * 32;
-constexpr int kScoreChunk = 32;  // logical pages per CTA
+constexpr int kScoreChunk = 64;  // logical pages per CTA
 
 struct ScoreParams {
   const uint16_t* summ;
@@ -71,12 +72,13 @@ __device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
   return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
-// Sum of v[j] over the 32 lanes for each j < G, then the max over j. The
-// halving steps leave lane l with head j(l); the final max is on all lanes.
-template <int G>
+// Sum of v[j] over the LPU lanes of a unit for each j < G, then the max over
+// j. The halving steps leave each lane with head j(lane) (bits of the lane
+// index); the final max is on every lane of the unit.
+template <int G, int LPU>
 __device__ __forceinline__ float group_bound_max(float (&v)[G], int lane) {
 #pragma unroll
-  for (int n = G, mask = 16; n > 1; n >>= 1, mask >>= 1) {
+  for (int n = G, mask = LPU / 2; n > 1; n >>= 1, mask >>= 1) {
     const bool up = (lane & mask) != 0;
 #pragma unroll
     for (int i = 0; i < n / 2; ++i) {
@@ -87,50 +89,52 @@ __device__ __forceinline__ float group_bound_max(float (&v)[G], int lane) {
   }
   float s = v[0];
 #pragma unroll
-  for (int mask = 16 / G; mask >= 1; mask >>= 1) s += __shfl_xor_sync(kFull, s, mask);
+  for (int mask = LPU / 2 / G; mask >= 1; mask >>= 1) s += __shfl_xor_sync(kFull, s, mask);
 #pragma unroll
-  for (int mask = 32 / G; mask <= 16; mask <<= 1) s = fmaxf(s, __shfl_xor_sync(kFull, s, mask));
+  for (int mask = LPU / G; mask <= LPU / 2; mask <<= 1)
+    s = fmaxf(s, __shfl_xor_sync(kFull, s, mask));
   return s;
 }
 
-// Lane slice of one (page, head) summary unit (min row then max row, 4d bytes):
-// 16 bytes (d=128) or 8 bytes (d=64).
-template <int D>
-struct UnitVec;
-template <>
-struct UnitVec<128> {
-  using T = uint4;
-};
-template <>
-struct UnitVec<64> {
-  using T = uint2;
+// One lane's slice of a (page, head) summary unit.
+template <int Bytes>
+struct Chunk {
+  uint4 v[Bytes / 16];
 };
 
-// CTA (x, y) = pages [32x, 32x+32) of request y. Warp w owns KV head w % Hkv and
-// every (8/Hkv)-th page of the chunk; one warp load of 32 lanes covers one
-// (page, head) unit exactly, and 4-8 pages are in flight per warp.
-template <int D, int G>
+// CTA (x, y) = pages [64x, 64x+64) of request y. Warp w owns KV head w % Hkv
+// and every (8/Hkv)-th page of the chunk. LPU lanes cover one (page, head)
+// unit (lanes [0, LPU/2) the min row with q-, the rest the max row with q+),
+// so a warp works on 32/LPU pages at once with coalesced 16-byte loads and
+// several page groups in flight. 16 lanes per unit halve the cross-lane
+// reduction of 32 while the group's queries still fit in registers.
+template <int D, int G, int LPU>
 __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(ScoreParams p) {
-  using V = typename UnitVec<D>::T;
-  constexpr int kCpl = D / 16;                             // channels per lane
-  constexpr int kScoreUnroll = (G * kCpl >= 64) ? 4 : 8;   // pages in flight per warp
+  constexpr int kVals = 2 * D / LPU;            // summary values (channels of one row) per lane
+  constexpr int kBpl = kVals * 2;               // bytes per lane per unit
+  constexpr int kPpi = 32 / LPU;                // pages per warp step
+  // pages in flight per lane: what fits in ~88 registers next to the queries
+  constexpr int kFit = (88 - G * kVals) / (kBpl / 4);
+  constexpr int kUnroll = kFit < 2 ? 2 : (kFit > 8 ? 8 : kFit);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int b = blockIdx.y;
   const int N = ceil_div(clamp_seq_len(p.seq_lens[b], p.max_pages, p.P, p.err), p.P);
   const int c0 = blockIdx.x * kScoreChunk;
   if (c0 >= N) return;
   const int head = warp % p.Hkv, wph = kScoreWarps / p.Hkv, sub = warp / p.Hkv;
-  const int part = lane >> 4;  // 0: min row, paired with q-; 1: max row, paired with q+
-  const int cl = (lane & 15) * kCpl;
+  const int ul = lane % LPU;                    // lane within the unit
+  const int part = ul >= LPU / 2;               // 0: min row (q-), 1: max row (q+)
+  const int cl = (ul % (LPU / 2)) * kVals;      // first channel of this lane
+  const int pslot = lane / LPU;                 // which of the kPpi pages of a step
 
   // the group's queries, sign part matching this lane's row, as fp32 pairs
-  uint64_t qv[G][kCpl / 2];
+  uint64_t qv[G][kVals / 2];
   {
     const float* qb = p.q + ((size_t)b * p.Hq + head * G) * D + cl;
 #pragma unroll
     for (int j = 0; j < G; ++j)
 #pragma unroll
-      for (int i = 0; i < kCpl; i += 4) {
+      for (int i = 0; i < kVals; i += 4) {
         const float4 x = *reinterpret_cast<const float4*>(qb + (size_t)j * D + i);
         const float a0 = part ? fmaxf(x.x, 0.f) : fminf(x.x, 0.f);
         const float a1 = part ? fmaxf(x.y, 0.f) : fminf(x.y, 0.f);
@@ -140,47 +144,63 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(ScoreParams p) 
         qv[j][i / 2 + 1] = pack2(a2, a3);
       }
   }
-  const int npg = min(kScoreChunk, N - c0);               // pages of this chunk
-  const int mine = (npg - sub + wph - 1) / wph;           // pages of this warp
+  const int npg = min(kScoreChunk, N - c0);     // pages of this chunk
+  const int mine = (npg - sub + wph - 1) / wph; // pages of this warp (<= 64)
   const int32_t* bt_row = p.bt + (size_t)b * p.max_pages + c0 + sub;
   float* out = p.scores + ((size_t)b * p.Hkv + head) * p.max_pages + c0 + sub;
-  const int unit_off = head * 4 * D + lane * (int)sizeof(V);  // bytes inside a page block
+  const int unit_off = head * 4 * D + part * 2 * D + cl * 2;  // bytes inside a page block
 
-  // block-table entries of this warp's pages: lane k holds page k
-  int phys = -1;
-  if (lane < mine) phys = __ldg(bt_row + lane * wph);
-  if (lane < mine && (phys < 0 || phys >= p.num_phys)) {
-    report(p.err, ASP_DEVERR_PAGE_RANGE);
-    phys = -1;
-  }
-  for (int k0 = 0; k0 < mine; k0 += kScoreUnroll) {
-    V x[kScoreUnroll];
+  // block-table entries of this warp's pages: lane k holds pages k and 32 + k
+  int phys[2] = {-1, -1};
 #pragma unroll
-    for (int u = 0; u < kScoreUnroll; ++u) {
-      const int ph = __shfl_sync(kFull, phys, (k0 + u) & 31);
-      if (k0 + u < mine && ph >= 0)
-        x[u] = __ldg(reinterpret_cast<const V*>(
-            reinterpret_cast<const uint8_t*>(p.summ) + (size_t)ph * p.Hkv * 4 * D + unit_off));
+  for (int r = 0; r < 2; ++r) {
+    const int k = r * 32 + lane;
+    if (k < mine) {
+      phys[r] = __ldg(bt_row + k * wph);
+      if (phys[r] < 0 || phys[r] >= p.num_phys) {
+        report(p.err, ASP_DEVERR_PAGE_RANGE);
+        phys[r] = -1;
+      }
+    }
+  }
+  auto phys_of = [&](int k) {  // physical page of this warp's page k < 64 (warp-wide call)
+    const int a = __shfl_sync(kFull, phys[0], k & 31);
+    const int c = __shfl_sync(kFull, phys[1], k & 31);
+    return k < 32 ? a : c;
+  };
+  for (int k0 = 0; k0 < mine; k0 += kPpi * kUnroll) {
+    Chunk<kBpl> x[kUnroll];
+    int ph[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int k = k0 + u * kPpi + pslot;
+      ph[u] = phys_of(min(k, 63));
+      if (k < mine && ph[u] >= 0) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            reinterpret_cast<const uint8_t*>(p.summ) + (size_t)ph[u] * p.Hkv * 4 * D + unit_off);
+#pragma unroll
+        for (int c = 0; c < kBpl / 16; ++c) x[u].v[c] = __ldg(src + c);
+      }
     }
 #pragma unroll
-    for (int u = 0; u < kScoreUnroll; ++u) {
-      if (k0 + u >= mine) break;  // warp-uniform
-      const int ph = __shfl_sync(kFull, phys, (k0 + u) & 31);
+    for (int u = 0; u < kUnroll; ++u) {
+      if (k0 + u * kPpi >= mine) break;  // warp-uniform
+      const int k = k0 + u * kPpi + pslot;
       const uint32_t* w = reinterpret_cast<const uint32_t*>(&x[u]);
-      uint64_t xv[kCpl / 2];
+      uint64_t xv[kVals / 2];
 #pragma unroll
-      for (int m = 0; m < kCpl / 2; ++m) xv[m] = bf16x2_to_f32x2(w[m]);
+      for (int m = 0; m < kVals / 2; ++m) xv[m] = bf16x2_to_f32x2(w[m]);
       float acc[G];
 #pragma unroll
       for (int j = 0; j < G; ++j) {
         uint64_t a2 = 0;
 #pragma unroll
-        for (int m = 0; m < kCpl / 2; ++m) a2 = ffma2(qv[j][m], xv[m], a2);
+        for (int m = 0; m < kVals / 2; ++m) a2 = ffma2(qv[j][m], xv[m], a2);
         const float2 f = unpack2(a2);
         acc[j] = f.x + f.y;
       }
-      const float sc = group_bound_max<G>(acc, lane) * p.inv_sqrt_d;
-      if (lane == 0) out[(k0 + u) * wph] = ph >= 0 ? sc : -INFINITY;
+      const float sc = group_bound_max<G, LPU>(acc, lane) * p.inv_sqrt_d;
+      if (ul == 0 && k < mine) out[k * wph] = ph[u] >= 0 ? sc : -INFINITY;
     }
   }
 }
@@ -459,7 +479,9 @@ cudaError_t launch_score_t(const SelectArgs& a, cudaStream_t stream) {
                 kv.batch, kv.num_q_heads, kv.num_kv_heads, kv.page_size, kv.max_pages,
                 kv.num_phys_pages, 1.0f / sqrtf((float)D)};
   dim3 grid(ceil_div(kv.max_pages, kScoreChunk), kv.batch);
-  score_kernel<D, G><<<grid, kScoreThreads, 0, stream>>>(p);
+  // 16 lanes per unit while the group's queries fit in 64 registers, else 32
+  constexpr int kLpu = (G * 2 * D / 16 > 64) ? 32 : 16;
+  score_kernel<D, G, kLpu><<<grid, kScoreThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
