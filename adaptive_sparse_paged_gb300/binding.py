@@ -34,6 +34,7 @@ EXPORTED = (
     "asp_coverage_select",
     "asp_sparse_decode",
     "asp_get_device_error",
+    "asp_coverage_select_noalloc",
 )
 
 
@@ -86,6 +87,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "asp_coverage_select": ([kvp, vp, ctypes.c_float, i32, vp, vp, vp, sz, vp], i32),
             "asp_sparse_decode": ([kvp, vp, vp, vp, ctypes.c_float, vp, vp, vp, sz, vp], i32),
             "asp_get_device_error": ([vp, u32p, vp], i32),
+            "asp_coverage_select_noalloc": ([kvp, vp, ctypes.c_float, i32, vp, vp, vp, vp], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -229,6 +231,29 @@ def asp_sparse_decode(kv: PagedKV, q: torch.Tensor, lists: torch.Tensor, lens: t
             kv.ref, q.data_ptr(), lists.data_ptr(), lens.data_ptr(), ctypes.c_float(sm_scale),
             out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(),
             _stream_ptr(kv.device, stream)), "asp_sparse_decode")
+
+
+def asp_coverage_select_noalloc(kv: PagedKV, q: torch.Tensor, gamma: float, budget: int,
+                                lists: torch.Tensor, lens: torch.Tensor,
+                                dev_error: torch.Tensor | None = None, stream=None) -> None:
+    """asp_coverage_select with the library's own fixed scratch instead of a workspace.
+
+    For callers that cannot allocate device memory; see include/asp.h for the
+    size limit and the rule that overlapping calls must be serialised.
+    dev_error: optional int32 [1] device tensor that collects device error bits.
+    """
+    _need(q, "q", torch.float32, kv.device, (kv.batch, kv.num_q_heads, kv.head_dim))
+    _need(lists, "lists", torch.int32, kv.device, (kv.batch, kv.num_kv_heads, kv.max_pages))
+    _need(lens, "lens", torch.int32, kv.device, (kv.batch, kv.num_kv_heads))
+    err_ptr = None
+    if dev_error is not None:
+        _need(dev_error, "dev_error", torch.int32, kv.device, (1,))
+        err_ptr = dev_error.data_ptr()
+    with torch.cuda.device(kv.device):
+        _check(load_library().asp_coverage_select_noalloc(
+            kv.ref, q.data_ptr(), ctypes.c_float(gamma), int(budget), lists.data_ptr(),
+            lens.data_ptr(), err_ptr, _stream_ptr(kv.device, stream)),
+            "asp_coverage_select_noalloc")
 
 
 def asp_get_device_error(ws: torch.Tensor, stream=None) -> int:

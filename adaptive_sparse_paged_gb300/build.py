@@ -20,7 +20,7 @@ ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG_DIR, "libasp.so")
-SOURCES = ["abi.cu", "summarize.cu", "select.cu", "decode.cu"]
+SOURCES = ["abi.cu", "summarize.cu", "select.cu", "decode.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -191,6 +191,30 @@ asp_status asp_sparse_decode(const asp_paged_kv* kv, const float* q,
                              void* ws, size_t ws_bytes, asp_stream stream);
 
 /*
+ * asp_coverage_select without a workspace. The paper has no counterpart: this
+ * entry point exists for callers that cannot allocate device memory, such as
+ * an engine that owns all GPU memory through its own pool and passes plugins
+ * only their input and output buffers, or a loop that must not allocate once
+ * running. It computes exactly what asp_coverage_select computes (same
+ * kernels, same arguments and outputs) and calls no allocating routine.
+ *
+ * Its scratch (the per-page scores) is a fixed array inside libasp.so that
+ * every GPU loading the library holds until exit: 4 MiB + 256 B. Shapes with
+ * batch * num_kv_heads * max_pages > ASP_NOALLOC_MAX_SCORES are rejected with
+ * ASP_EUNSUPPORTED before any device work. The first call on each device
+ * looks up the array's device address (cudaGetSymbolAddress with that device
+ * current); make that first call before any stream capture. All calls share
+ * the array and it keeps the last call's contents; calls that overlap on the
+ * GPU (other streams, other host threads) race on it, so serialise them.
+ * dev_error: optional device word (may be NULL); device-detected range
+ * problems are OR-ed into it as ASP_DEVERR_* bits; the caller clears it.
+ */
+#define ASP_NOALLOC_MAX_SCORES (1u << 20)
+asp_status asp_coverage_select_noalloc(const asp_paged_kv* kv, const float* q, float gamma,
+                                       int32_t budget, int32_t* lists, int32_t* lens,
+                                       uint32_t* dev_error, asp_stream stream);
+
+/*
  * Synchronises `stream`, copies the device error word into *code_out
  * (0 = none; else a mask of ASP_DEVERR_* bits), clears it and returns
  * ASP_EDEVICE if it was non-zero, else ASP_OK. After an error, call
