@@ -9,9 +9,11 @@
 // Shares differ by at most one page whatever the length mix. A CTA's range
 // cuts at most two segments; each (segment, CTA) piece produces one partial
 // (m, l, o) in slot segment + CTA of the workspace, which is unique because
-// both indices grow along the sequence. A per-segment counter elects the last
-// CTA to finish a segment; it merges the partials by log-sum-exp and resets
-// the counter, so nothing ever waits on another CTA.
+// both indices grow along the sequence; a segment held whole by one CTA is
+// written out directly. A small second kernel merges the split segments by
+// log-sum-exp. The streaming kernel thus never fences, counts or waits on
+// another CTA: under full HBM load each such round trip costs 1.5-2 us, and
+// at a piece end it would stall that CTA's copy pipeline.
 //
 // Data path (per CTA: 8 warps, one CTA per SM): every warp runs its own
 // pipeline. Warp w takes stages w, w+8, ... of the CTA's slice (a stage is a
@@ -199,6 +201,18 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       p.out[((size_t)b * p.Hq + h * p.g + e / D) * D + e % D] = 0.f;
     for (int e = tid; e < p.g; e += kDecThreads) p.lse[(size_t)b * p.Hq + h * p.g + e] = -INFINITY;
   }
+  // Merge table for the merge kernel: entry s = (first CTA << 16) | last CTA
+  // holding a piece of segment s; equal halves mean nothing to merge.
+  if (cta == 0) {
+    for (int s = tid; s < S; s += kDecThreads) {
+      int t = 0;
+      if (prefix[s + 1] > prefix[s]) {
+        const int cf = cta_of(prefix[s], total, geff), cl = cta_of(prefix[s + 1] - 1, total, geff);
+        t = (cf << 16) | cl;
+      }
+      p.counters[s] = t;
+    }
+  }
   if (beg >= end) return;
   if (tid == 0) {
     prefetch_tensormap(&tmK);
@@ -300,32 +314,34 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const int gid = lane >> 2, tq = lane & 3;
   int nc = 0;      // next warp stage to consume
   int waited = 0;  // stages whose copies are known complete
+  // Q^T fragments (B operand): rows d = kk*16 + 2*tq (+1, +8, +9), column gid
+  uint32_t qhi[D / 16][2], qlo[D / 16][2];
+  auto load_q = [&](int seg) {
+    const int qb = seg / p.Hkv, qh = seg % p.Hkv;
+    const bool live = gid < p.g;
+    const float* qr = p.q + ((size_t)qb * p.Hq + qh * p.g + (live ? gid : 0)) * D;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float2 v = make_float2(0.f, 0.f);
+        if (live) v = *reinterpret_cast<const float2*>(qr + kk * 16 + half * 8 + 2 * tq);
+        v.x *= p.scale_log2;
+        v.y *= p.scale_log2;
+        const __nv_bfloat162 hv = __floats2bfloat162_rn(v.x, v.y);
+        const float2 hf = __bfloat1622float2(hv);
+        qhi[kk][half] = *reinterpret_cast<const uint32_t*>(&hv);
+        qlo[kk][half] = pack_bf16(v.x - hf.x, v.y - hf.y);
+      }
+  };
   long long pos = beg;
+  load_q(seg_of(prefix, S, (int)pos));
   while (pos < end) {
     const int s = seg_of(prefix, S, (int)pos);
     const long long seg_lo = prefix[s], seg_hi = prefix[s + 1];
     const long long pe = seg_hi < end ? seg_hi : end;
     const int b = s / p.Hkv, h = s % p.Hkv;
 
-    // Q^T fragments (B operand): rows d = kk*16 + 2*tq (+1, +8, +9), column gid
-    uint32_t qhi[D / 16][2], qlo[D / 16][2];
-    {
-      const bool live = gid < p.g;
-      const float* qr = p.q + ((size_t)b * p.Hq + h * p.g + (live ? gid : 0)) * D;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float2 v = make_float2(0.f, 0.f);
-          if (live) v = *reinterpret_cast<const float2*>(qr + kk * 16 + half * 8 + 2 * tq);
-          v.x *= p.scale_log2;
-          v.y *= p.scale_log2;
-          const __nv_bfloat162 hv = __floats2bfloat162_rn(v.x, v.y);
-          const float2 hf = __bfloat1622float2(hv);
-          qhi[kk][half] = *reinterpret_cast<const uint32_t*>(&hv);
-          qlo[kk][half] = pack_bf16(v.x - hf.x, v.y - hf.y);
-        }
-    }
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     float o[D / 16][4];
 #pragma unroll
@@ -444,6 +460,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       mw[16 + (2 * tq) * D + d0 + 8] = o[dt][2];
       mw[16 + (2 * tq + 1) * D + d0 + 8] = o[dt][3];
     }
+    if (pe < end) load_q(seg_of(prefix, S, (int)pe));  // next piece's queries overlap the merge
     __syncthreads();
     const bool whole = (pos == seg_lo) && (pe == seg_hi);
     float* pslot = p.partials + (size_t)(s + cta) * p.slot_floats;
@@ -474,48 +491,67 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
       }
     }
-    if (!whole) {
-      __threadfence();
-      __syncthreads();
-      if (tid == 0) {
-        const int cf = cta_of(seg_lo, total, geff), cl = cta_of(seg_hi - 1, total, geff);
-        const int prev = atomicAdd(&p.counters[s], 1);
-        const int last = prev == cl - cf;
-        if (last) p.counters[s] = 0;
-        flags[0] = last ? 1 : 0;
-        flags[1] = cf;
-        flags[2] = cl;
-      }
-      __syncthreads();
-      if (flags[0]) {
-        __threadfence();
-        const int cf = flags[1], cl = flags[2];
-        for (int e = tid; e < p.g * D; e += kDecThreads) {
-          const int col = e / D, d = e % D;
-          float M = -INFINITY;
-          for (int c = cf; c <= cl; ++c)
-            M = fmaxf(M, __ldcg(p.partials + (size_t)(s + c) * p.slot_floats + col));
-          float L = 0.f, acc = 0.f;
-          if (M != -INFINITY) {
-            for (int c = cf; c <= cl; ++c) {
-              const float* q = p.partials + (size_t)(s + c) * p.slot_floats;
-              const float sc = exp2f(__ldcg(q + col) - M);
-              L += sc * __ldcg(q + 8 + col);
-              acc += sc * __ldcg(q + 16 + col * D + d);
-            }
-          }
-          const size_t row = (size_t)b * p.Hq + h * p.g + col;
-          p.out[row * D + d] = L > 0.f ? acc / L : 0.f;
-          if (d == 0) p.lse[row] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
-        }
-      }
-    }
     __syncthreads();  // the merge area is rewritten by the next piece
     pos = pe;
   }
   // never leave the CTA with copies in flight (only after a timeout can any remain)
   if (lane == 0)
     for (int n = waited; n < ni; ++n) mbar_wait(&my_full[n % C::kSlots], (n / C::kSlots) & 1);
+}
+
+// Merges the partials of every segment that the decode kernel split across
+// CTAs (one CTA per segment; segments held by one CTA exit at once). Pieces
+// are combined in CTA order, so the result does not depend on timing.
+struct MergeParams {
+  const float* partials;
+  const int32_t* table;
+  float* out;
+  float* lse;
+  int Hq, Hkv, g, D, slot_floats;
+};
+
+__global__ void __launch_bounds__(1024) merge_kernel(const MergeParams p) {
+  extern __shared__ float ms[];  // [np][8] weights, [np][8] l, M[8], L[8]
+  const int s = blockIdx.x, tid = threadIdx.x;
+  const int t = p.table[s];
+  const int cf = t >> 16, cl = t & 0xffff;
+  if (cf >= cl) return;
+  const int np = cl - cf + 1;
+  float* wm = ms;
+  float* wl = ms + np * 8;
+  float* ml = ms + np * 16;
+  for (int e = tid; e < np * 8; e += blockDim.x) {
+    const float* q = p.partials + (size_t)(s + cf + e / 8) * p.slot_floats;
+    wm[e] = q[e % 8];
+    wl[e] = q[8 + (e % 8)];
+  }
+  __syncthreads();
+  if (tid < p.g) {
+    float M = -INFINITY;
+    for (int c = 0; c < np; ++c) M = fmaxf(M, wm[c * 8 + tid]);
+    float L = 0.f;
+    for (int c = 0; c < np; ++c) {
+      const float w = M == -INFINITY ? 0.f : exp2f(wm[c * 8 + tid] - M);
+      wm[c * 8 + tid] = w;
+      L += w * wl[c * 8 + tid];
+    }
+    ml[tid] = M;
+    ml[8 + tid] = L;
+  }
+  __syncthreads();
+  // one thread per output element; the piece loads are independent
+  const int b = s / p.Hkv, h = s % p.Hkv, D = p.D;
+  if (tid < p.g * D) {
+    const int col = tid / D, d = tid % D;
+    const float* src = p.partials + (size_t)(s + cf) * p.slot_floats + 16 + col * D + d;
+    float acc = 0.f;
+#pragma unroll 16
+    for (int c = 0; c < np; ++c) acc += wm[c * 8 + col] * src[(size_t)c * p.slot_floats];
+    const float M = ml[col], L = ml[8 + col];
+    const size_t row = (size_t)b * p.Hq + h * p.g + col;
+    p.out[row * D + d] = L > 0.f ? acc / L : 0.f;
+    if (d == 0) p.lse[row] = L > 0.f ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
+  }
 }
 
 // ----------------------------------------------------------------- host side
@@ -565,6 +601,12 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
               kv.num_q_heads / kv.num_kv_heads, kv.max_pages, kv.num_phys_pages, a.slot_floats,
               a.sm_scale * 1.4426950408889634f};
   decode_kernel<D, P><<<a.grid, kDecThreads, smem, stream>>>(tk, tv, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  MergeParams mp{a.partials, a.counters, a.out, a.lse, kv.num_q_heads, kv.num_kv_heads,
+                 kv.num_q_heads / kv.num_kv_heads, D, a.slot_floats};
+  const size_t msmem = ((size_t)a.grid * 16 + 16) * sizeof(float);
+  if ((e = set_max_dynamic_smem((const void*)merge_kernel, (int)msmem)) != cudaSuccess) return e;
+  merge_kernel<<<S, (kv.num_q_heads / kv.num_kv_heads) * D, msmem, stream>>>(mp);
   return cudaGetLastError();
 }
 

@@ -211,6 +211,7 @@ constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelCache = 8192;  // scores cached in shared memory when N fits
 constexpr int kBins = 256;
 constexpr int kLimbBits = 13;    // mass = l0 + l1 << 13 + l2 << 26, each limb < 2^13
+constexpr int kWarpCand = 4096;  // candidates one warp finishes on (fits the histogram area)
 constexpr size_t kSelSmem = (size_t)kSelWarps * kBins * 4 * sizeof(uint32_t) +  // private hists
                             kSelCache * sizeof(float);                            // score cache
 
@@ -322,10 +323,73 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
   uint32_t above_c = 0, cnt_eq = 0;
   uint32_t* my_hist = hist + warp * kBins * 4;
   constexpr uint32_t kLimbMask = (1u << kLimbBits) - 1u;
-  while (true) {
+  // warp 0: lane owns bins [8*lane, 8*lane+8) of m_cnt/m_mass; finds the
+  // largest bin j with above + (sum over bins >= j) >= target
+  auto pick_bin = [&]() {
+    unsigned long long lm = 0;
+    uint32_t lc = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      lm += m_mass[lane * 8 + i];
+      lc += m_cnt[lane * 8 + i];
+    }
+    unsigned long long sm = lm;  // inclusive suffix over lanes >= lane
+    uint32_t scn = lc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long ym = __shfl_down_sync(kFull, sm, o);
+      const uint32_t yc = __shfl_down_sync(kFull, scn, o);
+      if (lane + o < 32) {
+        sm += ym;
+        scn += yc;
+      }
+    }
+    const bool reach = mass_mode ? (above_m + sm >= target)
+                                 : ((unsigned long long)above_c + scn >= target);
+    const unsigned ballot = __ballot_sync(kFull, reach);
+    const int lstar = ballot ? 31 - __clz(ballot) : 0;  // lane 0 reaches by the invariant
+    if (lane == lstar) {
+      unsigned long long run_m = above_m + (sm - lm);
+      uint32_t run_c = above_c + (scn - lc);
+      int j = lane * 8;
+      for (int i = 7; i >= 0; --i) {
+        const int bin = lane * 8 + i;
+        const unsigned long long nm = run_m + m_mass[bin];
+        const uint32_t nc = run_c + m_cnt[bin];
+        if (mass_mode ? (nm >= target) : ((unsigned long long)nc >= target)) {
+          j = bin;
+          break;
+        }
+        run_m = nm;
+        run_c = nc;
+      }
+      pick[0] = (uint32_t)j;
+      pick[1] = run_c;
+      pick[2] = m_cnt[j];
+      pick_m[0] = run_m;
+    }
+  };
+  // narrows [lo, hi] to the picked bin; returns the shift the round used
+  auto narrow = [&](int shift) {
+    const uint32_t j = pick[0];
+    above_c = pick[1];
+    cnt_eq = pick[2];
+    above_m = pick_m[0];
+    const unsigned long long nlo = (unsigned long long)lo + ((unsigned long long)j << shift);
+    const unsigned long long nhi = nlo + ((1ull << shift) - 1ull);
+    lo = (uint32_t)nlo;
+    hi = nhi < hi ? (uint32_t)nhi : hi;
+  };
+  auto shift_of = [&]() {
     const uint32_t range = hi - lo;
     const int bits = range ? 32 - __clz(range) : 0;
-    const int shift = bits > 8 ? bits - 8 : 0;
+    return bits > 8 ? bits - 8 : 0;
+  };
+
+  // Block-wide rounds over every element while the picked bin is large.
+  bool resolved = false;
+  while (true) {
+    const int shift = shift_of();
     for (int i = tid; i < kSelWarps * kBins; i += kSelThreads)
       reinterpret_cast<uint4*>(hist)[i] = make_uint4(0, 0, 0, 0);
     __syncthreads();
@@ -358,63 +422,75 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
       m_mass[tid] = l0 + (l1 << kLimbBits) + (l2 << (2 * kLimbBits));
     }
     __syncthreads();
+    if (warp == 0) pick_bin();
+    __syncthreads();
+    narrow(shift);
+    if (shift == 0) {
+      resolved = true;
+      break;
+    }
+    if (cnt_eq <= kWarpCand) break;  // few candidates left: one warp finishes
+    __syncthreads();
+  }
+  if (!resolved) {
+    // gather the candidates (scores with keys in [lo, hi]) and let warp 0
+    // run the remaining rounds on them with warp-level synchronisation only
+    float* cand = reinterpret_cast<float*>(hist + kBins * 4);  // after warp 0's histogram
+    if (tid == 0) pick[3] = 0;
+    __syncthreads();
+    for (int i = tid; i < N; i += kSelThreads) {
+      const float v = sc[i];
+      const uint32_t k = score_key(v);
+      if (k >= lo && k <= hi) cand[atomicAdd(&pick[3], 1u)] = v;
+    }
+    __syncthreads();
     if (warp == 0) {
-      // lane owns bins [8*lane, 8*lane+8); find the largest bin j with
-      // above + (sum over bins >= j) >= target
-      unsigned long long lm = 0;
-      uint32_t lc = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        lm += m_mass[lane * 8 + i];
-        lc += m_cnt[lane * 8 + i];
-      }
-      unsigned long long sm = lm;  // inclusive suffix over lanes >= lane
-      uint32_t scn = lc;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long ym = __shfl_down_sync(kFull, sm, o);
-        const uint32_t yc = __shfl_down_sync(kFull, scn, o);
-        if (lane + o < 32) {
-          sm += ym;
-          scn += yc;
-        }
-      }
-      const bool reach = mass_mode ? (above_m + sm >= target)
-                                   : ((unsigned long long)above_c + scn >= target);
-      const unsigned ballot = __ballot_sync(kFull, reach);
-      const int lstar = ballot ? 31 - __clz(ballot) : 0;  // lane 0 reaches by the invariant
-      if (lane == lstar) {
-        unsigned long long run_m = above_m + (sm - lm);
-        uint32_t run_c = above_c + (scn - lc);
-        int j = lane * 8;
-        for (int i = 7; i >= 0; --i) {
-          const int bin = lane * 8 + i;
-          const unsigned long long nm = run_m + m_mass[bin];
-          const uint32_t nc = run_c + m_cnt[bin];
-          if (mass_mode ? (nm >= target) : ((unsigned long long)nc >= target)) {
-            j = bin;
-            break;
+      const int nc = (int)pick[3];
+      while (true) {
+        const int shift = shift_of();
+        for (int i = lane; i < kBins; i += 32)
+          reinterpret_cast<uint4*>(hist)[i] = make_uint4(0, 0, 0, 0);
+        __syncwarp();
+        for (int i = lane; i < nc; i += 32) {
+          const float v = cand[i];
+          const uint32_t k = score_key(v);
+          if (k >= lo && k <= hi) {
+            uint32_t* h = hist + ((k - lo) >> shift) * 4;
+            atomicAdd(h, 1u);
+            if (mass_mode) {
+              const unsigned long long m = mass_fixed(v, smax);
+              atomicAdd(h + 1, (uint32_t)m & kLimbMask);
+              atomicAdd(h + 2, (uint32_t)(m >> kLimbBits) & kLimbMask);
+              atomicAdd(h + 3, (uint32_t)(m >> (2 * kLimbBits)));
+            }
           }
-          run_m = nm;
-          run_c = nc;
         }
-        pick[0] = (uint32_t)j;
-        pick[1] = run_c;
-        pick[2] = m_cnt[j];
-        pick_m[0] = run_m;
+        __syncwarp();
+        for (int i = lane; i < kBins; i += 32) {
+          const uint4 h = reinterpret_cast<const uint4*>(hist)[i];
+          m_cnt[i] = h.x;
+          m_mass[i] = (unsigned long long)h.y + ((unsigned long long)h.z << kLimbBits) +
+                      ((unsigned long long)h.w << (2 * kLimbBits));
+        }
+        __syncwarp();
+        pick_bin();
+        __syncwarp();
+        narrow(shift);
+        __syncwarp();
+        if (shift == 0) break;
+      }
+      if (lane == 0) {  // publish the result for the whole block
+        pick[0] = lo;
+        pick[1] = above_c;
+        pick[2] = cnt_eq;
+        pick_m[0] = above_m;
       }
     }
     __syncthreads();
-    const uint32_t j = pick[0];
+    lo = pick[0];
     above_c = pick[1];
     cnt_eq = pick[2];
     above_m = pick_m[0];
-    const unsigned long long nlo = (unsigned long long)lo + ((unsigned long long)j << shift);
-    const unsigned long long nhi = nlo + ((1ull << shift) - 1ull);
-    lo = (uint32_t)nlo;
-    hi = nhi < hi ? (uint32_t)nhi : hi;
-    __syncthreads();
-    if (shift == 0) break;
   }
   const uint32_t tau = lo;
   // ties at the cutoff key: keep the first t (lowest ids)

@@ -43,11 +43,12 @@ class DecodeStep:
         self.ws = B.new_workspace(kv0)
         self.graph = None
 
-    # kernel launches of one step: (select: score + select, decode) per layer (+ append)
+    # kernel launches of one step, per layer: score + select (select alone at
+    # gamma = 1), decode + merge, and the append kernel when enabled
     @property
     def launches_per_step(self) -> int:
         per = 2 if (self.budget > 0 or self.gamma < 1.0) else 1
-        return len(self.kvs) * (per + 1 + (1 if self.append is not None else 0))
+        return len(self.kvs) * (per + 2 + (1 if self.append is not None else 0))
 
     def run_layer(self, l: int, stream=None, events=None):
         kv = self.kvs[l]
