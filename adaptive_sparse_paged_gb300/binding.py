@@ -132,7 +132,7 @@ class PagedKV:
     """One layer's paged cache (device tensors), mirrored into asp_paged_kv.
 
     k_cache, v_cache : bf16 [num_phys_pages, Hkv, P, d]
-    summaries        : bf16 [num_phys_pages, Hkv, 2, d]
+    summaries        : bf16 [B, Hkv, max_pages, 2, d], logical page order
     block_table      : int32 [B, max_pages]
     seq_lens         : int32 [B]
     num_q_heads      : Hq (query head h reads KV head h // (Hq // Hkv))
@@ -151,9 +151,9 @@ class PagedKV:
         n, hkv, p, d = self.k_cache.shape
         _need(self.k_cache, "k_cache", torch.bfloat16, dev)
         _need(self.v_cache, "v_cache", torch.bfloat16, dev, (n, hkv, p, d))
-        _need(self.summaries, "summaries", torch.bfloat16, dev, (n, hkv, 2, d))
         _need(self.block_table, "block_table", torch.int32, dev)
         b, max_pages = self.block_table.shape
+        _need(self.summaries, "summaries", torch.bfloat16, dev, (b, hkv, max_pages, 2, d))
         _need(self.seq_lens, "seq_lens", torch.int32, dev, (b,))
         self.device = dev
         self.batch, self.num_kv_heads, self.page_size, self.head_dim = b, hkv, p, d
@@ -166,6 +166,13 @@ class PagedKV:
     @property
     def ref(self):
         return ctypes.byref(self.struct)
+
+
+def new_summaries(k_cache: torch.Tensor, block_table: torch.Tensor) -> torch.Tensor:
+    """Zeroed summaries tensor [B, Hkv, max_pages, 2, d] for this cache and table."""
+    _, hkv, _, d = k_cache.shape
+    b, max_pages = block_table.shape
+    return torch.zeros((b, hkv, max_pages, 2, d), dtype=torch.bfloat16, device=k_cache.device)
 
 
 # ----------------------------------------------------------- C-ABI mirrors

@@ -29,7 +29,7 @@ asp_status check_kv(const asp_paged_kv* kv) {
   if ((long long)kv->batch * kv->num_kv_heads > kMaxSegments) return ASP_EUNSUPPORTED;
   if (kv->max_pages > kMaxPages) return ASP_EUNSUPPORTED;
   // page-space and TMA row coordinates are int32
-  if ((long long)kv->batch * kv->max_pages >= (1LL << 31)) return ASP_EUNSUPPORTED;
+  if ((long long)kv->batch * kv->num_kv_heads * kv->max_pages >= (1LL << 31)) return ASP_EUNSUPPORTED;
   if ((long long)kv->num_phys_pages * kv->num_kv_heads * kv->page_size >= (1LL << 31))
     return ASP_EUNSUPPORTED;
   // 16-byte alignment of the cache bases (bulk and tensor copies)
@@ -118,8 +118,8 @@ asp_status asp_workspace_size(const asp_paged_kv* kv, size_t* bytes) {
 
 asp_status asp_workspace_init(void* ws, size_t ws_bytes, asp_stream stream) {
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < 256) return ASP_EWORKSPACE;
-  // the error word and every counter live before the scores; zeroing the
-  // whole buffer is simplest and still cheap
+  // only the error word has to start at zero; zeroing the whole buffer is
+  // simplest and still cheap
   return from_cuda(cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream)));
 }
 
@@ -173,7 +173,7 @@ asp_status asp_sparse_decode(const asp_paged_kv* kv, const float* q, const int32
   uint8_t* w = static_cast<uint8_t*>(ws);
   DecodeArgs a{kv, q, lists, lens, sm_scale, out, lse,
                reinterpret_cast<float*>(w + lay.partials_off),
-               reinterpret_cast<int32_t*>(w + lay.counters_off), reinterpret_cast<uint32_t*>(w),
+               reinterpret_cast<int32_t*>(w + lay.table_off), reinterpret_cast<uint32_t*>(w),
                lay.decode_grid, lay.slot_floats};
   return from_cuda(launch_decode(a, static_cast<cudaStream_t>(stream)));
 }

@@ -74,7 +74,7 @@ struct DecParams {
   float* out;
   float* lse;
   float* partials;
-  int32_t* counters;
+  int32_t* merge_table;
   uint32_t* err;
   int B, Hq, Hkv, g, max_pages, num_phys, slot_floats;
   float scale_log2;
@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const int cf = cta_of(prefix[s], total, geff), cl = cta_of(prefix[s + 1] - 1, total, geff);
         t = (cf << 16) | cl;
       }
-      p.counters[s] = t;
+      p.merge_table[s] = t;
     }
   }
   if (beg >= end) return;
@@ -597,12 +597,12 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
   if ((e = make_page_map(&tk, kv.k_cache, rows, D, P)) != cudaSuccess) return e;
   if ((e = make_page_map(&tv, kv.v_cache, rows, D, P)) != cudaSuccess) return e;
   DecParams p{a.q, a.lists, a.lens, kv.block_table, kv.seq_lens, a.out, a.lse, a.partials,
-              a.counters, a.err, kv.batch, kv.num_q_heads, kv.num_kv_heads,
+              a.merge_table, a.err, kv.batch, kv.num_q_heads, kv.num_kv_heads,
               kv.num_q_heads / kv.num_kv_heads, kv.max_pages, kv.num_phys_pages, a.slot_floats,
               a.sm_scale * 1.4426950408889634f};
   decode_kernel<D, P><<<a.grid, kDecThreads, smem, stream>>>(tk, tv, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  MergeParams mp{a.partials, a.counters, a.out, a.lse, kv.num_q_heads, kv.num_kv_heads,
+  MergeParams mp{a.partials, a.merge_table, a.out, a.lse, kv.num_q_heads, kv.num_kv_heads,
                  kv.num_q_heads / kv.num_kv_heads, D, a.slot_floats};
   const size_t msmem = ((size_t)a.grid * 16 + 16) * sizeof(float);
   if ((e = set_max_dynamic_smem((const void*)merge_kernel, (int)msmem)) != cudaSuccess) return e;

@@ -2,22 +2,22 @@
 // head and step, keep the smallest page set whose estimated attention mass
 // reaches gamma). Two kernels:
 //
-// score_kernel   HBM-bound stream over the page summaries. A CTA takes 64
-//                logical pages of one request; warp w owns KV head w % Hkv.
-//                16 lanes (32 when the group's queries would not fit in
-//                registers) cover one (page, head) unit with coalesced
-//                16-byte loads, several pages in flight per warp. A lane
-//                holds channels of either the min row or the max row,
-//                together with the matching sign part of the group's
-//                queries, so
+// score_kernel   HBM-bound stream over the page summaries, which are kept in
+//                logical page order per (request, KV head) segment. Every
+//                warp of a persistent grid streams its own even slice of all
+//                segments' pages with 4 KiB bulk copies into a private
+//                3-slot ring. 16 lanes (32 when the group's queries would
+//                not fit in registers) score one page. A lane holds channels
+//                of either the min row or the max row, together with the
+//                matching sign part of the group's queries, so
 //                sum_i max(q_i*mn_i, q_i*mx_i) = sum_i q-_i*mn_i + q+_i*mx_i
 //                is one fp32 FMA per element (paired with fma.rn.f32x2). A
 //                transpose-reduce leaves each head's sum on a lane group; the
 //                group max times 1/sqrt(d) is the page score. Scores stay
 //                fp32: bf16 queries would move them by ~1e-3 and change lists.
-//                (Plain 16-byte loads from many warps reach the copy
-//                bandwidth on this gather; a single-thread bulk-copy ring per
-//                CTA does not.)
+//                (Gathering 512-byte per-(page, head) summaries scattered by
+//                the block table runs at under half the copy bandwidth;
+//                contiguous 4 KiB runs reach it.)
 //
 // select_kernel  One CTA per segment. Softmax weights exp(s - max) are turned
 //                into fixed point (2^38 = weight of the top page), so every
@@ -39,16 +39,14 @@ constexpr unsigned kFull = 0xffffffffu;
 // ============================================================== score kernel
 constexpr int kScoreWarps = 8;
 constexpr int kScoreThreads = kScoreWarps * 32;
-constexpr int kScoreChunk = 64;  // logical pages per CTA
 
 struct ScoreParams {
   const uint16_t* summ;
   const float* q;
-  const int32_t* bt;
   const int32_t* seq_lens;
   float* scores;
   uint32_t* err;
-  int B, Hq, Hkv, P, max_pages, num_phys;
+  int B, Hq, Hkv, P, max_pages;
   float inv_sqrt_d;
 };
 
@@ -96,113 +94,195 @@ __device__ __forceinline__ float group_bound_max(float (&v)[G], int lane) {
   return s;
 }
 
-// One lane's slice of a (page, head) summary unit.
+// One lane's slice of a page's summary.
 template <int Bytes>
 struct Chunk {
   uint4 v[Bytes / 16];
 };
 
-// CTA (x, y) = pages [64x, 64x+64) of request y. Warp w owns KV head w % Hkv
-// and every (8/Hkv)-th page of the chunk. LPU lanes cover one (page, head)
-// unit (lanes [0, LPU/2) the min row with q-, the rest the max row with q+),
-// so a warp works on 32/LPU pages at once with coalesced 16-byte loads and
-// several page groups in flight. 16 lanes per unit halve the cross-lane
-// reduction of 32 while the group's queries still fit in registers.
+// Summaries are stored per segment (request b, KV head h) in logical page
+// order, so this pass is one sequential stream with no block-table lookups.
+// The concatenated page space of all segments (segment-major) is split evenly
+// over the warps of a persistent grid. Each warp walks its slice as pieces of
+// up to kPieceBytes (whole pages of one segment); lane 0 bulk-copies every
+// piece into the warp's own ring of kScoreSlots slots, one mbarrier per slot,
+// so no warp ever waits on another. LPU lanes score one page (lanes
+// [0, LPU/2) take the min row with q-, the rest the max row with q+), 32 / LPU
+// pages per warp step.
+constexpr int kPieceBytes = 4096;
+constexpr int kScoreSlots = 3;
+
+template <int D, int LPU>
+struct ScoreCfg {
+  static constexpr int kVals = 2 * D / LPU;  // channels per lane (one row)
+  static constexpr int kBpl = kVals * 2;     // bytes per lane per page
+  static constexpr int kPpi = 32 / LPU;      // pages per warp step
+  static constexpr int kPageBytes = 4 * D;   // min and max rows of one page
+  static constexpr int kPiecePages = kPieceBytes / kPageBytes;
+};
+
+// Position in a warp's slice: segment (b, h), logical page lp, and the index
+// in the concatenated page space. Every lane of the warp holds the same one.
+struct SegCursor {
+  int b, h, lp, pos;
+};
+
 template <int D, int G, int LPU>
 __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(ScoreParams p) {
-  constexpr int kVals = 2 * D / LPU;            // summary values (channels of one row) per lane
-  constexpr int kBpl = kVals * 2;               // bytes per lane per unit
-  constexpr int kPpi = 32 / LPU;                // pages per warp step
-  // pages in flight per lane: what fits in ~88 registers next to the queries
-  constexpr int kFit = (88 - G * kVals) / (kBpl / 4);
-  constexpr int kUnroll = kFit < 2 ? 2 : (kFit > 8 ? 8 : kFit);
+  using C = ScoreCfg<D, LPU>;
+  constexpr int kVals = C::kVals, kBpl = C::kBpl, kPpi = C::kPpi;
+  constexpr int kPiecePages = C::kPiecePages, kPageBytes = C::kPageBytes;
+  extern __shared__ __align__(128) uint8_t score_smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int b = blockIdx.y;
-  const int N = ceil_div(clamp_seq_len(p.seq_lens[b], p.max_pages, p.P, p.err), p.P);
-  const int c0 = blockIdx.x * kScoreChunk;
-  if (c0 >= N) return;
-  const int head = warp % p.Hkv, wph = kScoreWarps / p.Hkv, sub = warp / p.Hkv;
-  const int ul = lane % LPU;                    // lane within the unit
-  const int part = ul >= LPU / 2;               // 0: min row (q-), 1: max row (q+)
-  const int cl = (ul % (LPU / 2)) * kVals;      // first channel of this lane
-  const int pslot = lane / LPU;                 // which of the kPpi pages of a step
+  constexpr int kRingBytes = kScoreWarps * kScoreSlots * kPieceBytes;
+  uint8_t* ring = score_smem + warp * kScoreSlots * kPieceBytes;  // this warp's slots
+  uint64_t* full = reinterpret_cast<uint64_t*>(score_smem + kRingBytes) + warp * kScoreSlots;
+  int* rprefix = reinterpret_cast<int*>(score_smem + kRingBytes +
+                                        kScoreWarps * kScoreSlots * sizeof(uint64_t));  // [B + 1]
 
-  // the group's queries, sign part matching this lane's row, as fp32 pairs
-  uint64_t qv[G][kVals / 2];
+  if (lane == 0) {
+    for (int i = 0; i < kScoreSlots; ++i) mbar_init(&full[i], 1);
+    mbar_fence_init();
+  }
+  // prefix of the requests' page counts N_b (clamped sequence lengths)
+  if (warp == 0) {
+    int carry = 0;
+    if (lane == 0) rprefix[0] = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+      const int b = b0 + lane;
+      int n = 0;
+      if (b < p.B) n = ceil_div(clamp_seq_len(p.seq_lens[b], p.max_pages, p.P, p.err), p.P);
+      int x = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
+      }
+      if (b < p.B) rprefix[b + 1] = carry + x;
+      carry += __shfl_sync(kFull, x, 31);
+    }
+  }
+  __syncthreads();
+  // this warp's slice of the Hkv * sum_b N_b pages (< 2^31, checked on the host)
+  const long long units = (long long)p.Hkv * rprefix[p.B];
+  const long long nw = (long long)gridDim.x * kScoreWarps;
+  const long long gw = (long long)blockIdx.x * kScoreWarps + warp;
+  const int wbeg = (int)(gw * units / nw), wend = (int)((gw + 1) * units / nw);
+  if (wbeg >= wend) return;
+
+  auto seg_pages = [&](int b) { return rprefix[b + 1] - rprefix[b]; };
+  SegCursor ic;  // issue cursor: the request holding page wbeg has N_b > 0
   {
-    const float* qb = p.q + ((size_t)b * p.Hq + head * G) * D + cl;
+    int lo = 0, hi = p.B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.Hkv * rprefix[mid] <= wbeg) lo = mid; else hi = mid - 1;
+    }
+    const int n = seg_pages(lo), off = wbeg - p.Hkv * rprefix[lo];
+    ic = SegCursor{lo, off / n, off % n, wbeg};
+  }
+  SegCursor cc = ic;  // consume cursor: the same sequence of pieces, later
+  auto piece_pages = [&](const SegCursor& c) {
+    return min(min(kPiecePages, seg_pages(c.b) - c.lp), wend - c.pos);
+  };
+  auto advance = [&](SegCursor& c, int n) {
+    c.pos += n;
+    c.lp += n;
+    if (c.lp == seg_pages(c.b)) {
+      c.lp = 0;
+      if (++c.h == p.Hkv) {
+        c.h = 0;
+        do ++c.b; while (c.b < p.B && seg_pages(c.b) == 0);
+      }
+    }
+  };
+  int issued = 0;
+  auto issue = [&]() {  // next piece of the slice into slot issued % kScoreSlots
+    const int n = piece_pages(ic);
+    if (lane == 0) {
+      const int slot = issued % kScoreSlots;
+      const size_t first = ((size_t)ic.b * p.Hkv + ic.h) * p.max_pages + ic.lp;
+      mbar_arrive_expect_tx(&full[slot], n * kPageBytes);
+      bulk_g2s(ring + slot * kPieceBytes,
+               reinterpret_cast<const uint8_t*>(p.summ) + first * kPageBytes, n * kPageBytes,
+               &full[slot]);
+    }
+    advance(ic, n);
+    ++issued;
+  };
+  for (int k = 0; k < kScoreSlots && ic.pos < wend; ++k) issue();
+
+  const int ul = lane % LPU, part = ul >= LPU / 2, ur = ul % (LPU / 2), pslot = lane / LPU;
+  // chunk c of this lane = bytes [(c * LPU/2 + ur) * 16, +16) of its row
+  const int lane_off = part * 2 * D + ur * 16;
+  uint64_t qv[G][kVals / 2];
+  auto load_q = [&](int b, int h) {
+    const float* qp = p.q + ((size_t)b * p.Hq + h * G) * D + ur * 8;
 #pragma unroll
-    for (int j = 0; j < G; ++j)
+    for (int jj = 0; jj < G; ++jj)
 #pragma unroll
-      for (int i = 0; i < kVals; i += 4) {
-        const float4 x = *reinterpret_cast<const float4*>(qb + (size_t)j * D + i);
+      for (int i = 0; i < kVals; i += 4) {  // chunk i/8 holds channels (i/8 * LPU/2 + ur) * 8 + [0, 8)
+        const float4 x = *reinterpret_cast<const float4*>(
+            qp + (size_t)jj * D + (i / 8) * (LPU / 2) * 8 + (i % 8));
         const float a0 = part ? fmaxf(x.x, 0.f) : fminf(x.x, 0.f);
         const float a1 = part ? fmaxf(x.y, 0.f) : fminf(x.y, 0.f);
         const float a2 = part ? fmaxf(x.z, 0.f) : fminf(x.z, 0.f);
         const float a3 = part ? fmaxf(x.w, 0.f) : fminf(x.w, 0.f);
-        qv[j][i / 2] = pack2(a0, a1);
-        qv[j][i / 2 + 1] = pack2(a2, a3);
+        qv[jj][i / 2] = pack2(a0, a1);
+        qv[jj][i / 2 + 1] = pack2(a2, a3);
       }
-  }
-  const int npg = min(kScoreChunk, N - c0);     // pages of this chunk
-  const int mine = (npg - sub + wph - 1) / wph; // pages of this warp (<= 64)
-  const int32_t* bt_row = p.bt + (size_t)b * p.max_pages + c0 + sub;
-  float* out = p.scores + ((size_t)b * p.Hkv + head) * p.max_pages + c0 + sub;
-  const int unit_off = head * 4 * D + part * 2 * D + cl * 2;  // bytes inside a page block
-
-  // block-table entries of this warp's pages: lane k holds pages k and 32 + k
-  int phys[2] = {-1, -1};
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int k = r * 32 + lane;
-    if (k < mine) {
-      phys[r] = __ldg(bt_row + k * wph);
-      if (phys[r] < 0 || phys[r] >= p.num_phys) {
-        report(p.err, ASP_DEVERR_PAGE_RANGE);
-        phys[r] = -1;
-      }
-    }
-  }
-  auto phys_of = [&](int k) {  // physical page of this warp's page k < 64 (warp-wide call)
-    const int a = __shfl_sync(kFull, phys[0], k & 31);
-    const int c = __shfl_sync(kFull, phys[1], k & 31);
-    return k < 32 ? a : c;
   };
-  for (int k0 = 0; k0 < mine; k0 += kPpi * kUnroll) {
-    Chunk<kBpl> x[kUnroll];
-    int ph[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int k = k0 + u * kPpi + pslot;
-      ph[u] = phys_of(min(k, 63));
-      if (k < mine && ph[u] >= 0) {
-        const uint4* src = reinterpret_cast<const uint4*>(
-            reinterpret_cast<const uint8_t*>(p.summ) + (size_t)ph[u] * p.Hkv * 4 * D + unit_off);
-#pragma unroll
-        for (int c = 0; c < kBpl / 16; ++c) x[u].v[c] = __ldg(src + c);
-      }
+  int qseg = -1, k = 0;
+  bool aborted = false;
+#pragma unroll 1
+  for (; cc.pos < wend; ++k) {
+    const int slot = k % kScoreSlots;
+    if (!__all_sync(kFull, mbar_wait(&full[slot], (k / kScoreSlots) & 1))) {
+      if (lane == 0) report(p.err, ASP_DEVERR_TIMEOUT);
+      aborted = true;
+      break;
     }
+    const int n = piece_pages(cc), seg = cc.b * p.Hkv + cc.h;
+    if (seg != qseg) {
+      load_q(cc.b, cc.h);
+      qseg = seg;
+    }
+    const uint8_t* sb = ring + slot * kPieceBytes + lane_off;
+    float* out = p.scores + (size_t)seg * p.max_pages + cc.lp;
+#pragma unroll 2
+    for (int i0 = 0; i0 < n; i0 += kPpi) {
+      const int pg = i0 + pslot;
+      const int pr = min(pg, n - 1);  // lanes past the piece re-read its last page
+      Chunk<kBpl> x;
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      if (k0 + u * kPpi >= mine) break;  // warp-uniform
-      const int k = k0 + u * kPpi + pslot;
-      const uint32_t* w = reinterpret_cast<const uint32_t*>(&x[u]);
+      for (int c = 0; c < kBpl / 16; ++c)
+        x.v[c] = *reinterpret_cast<const uint4*>(sb + pr * kPageBytes + c * (LPU / 2) * 16);
+      const uint32_t* w = reinterpret_cast<const uint32_t*>(&x);
       uint64_t xv[kVals / 2];
 #pragma unroll
       for (int m = 0; m < kVals / 2; ++m) xv[m] = bf16x2_to_f32x2(w[m]);
       float acc[G];
 #pragma unroll
-      for (int j = 0; j < G; ++j) {
+      for (int jj = 0; jj < G; ++jj) {
         uint64_t a2 = 0;
 #pragma unroll
-        for (int m = 0; m < kVals / 2; ++m) a2 = ffma2(qv[j][m], xv[m], a2);
+        for (int m = 0; m < kVals / 2; ++m) a2 = ffma2(qv[jj][m], xv[m], a2);
         const float2 f = unpack2(a2);
-        acc[j] = f.x + f.y;
+        acc[jj] = f.x + f.y;
       }
       const float sc = group_bound_max<G, LPU>(acc, lane) * p.inv_sqrt_d;
-      if (ul == 0 && k < mine) out[k * wph] = ph[u] >= 0 ? sc : -INFINITY;
+      if (ul == 0 && pg < n) out[pg] = sc;
+    }
+    advance(cc, n);
+    __syncwarp();  // every lane is done reading the slot
+    if (ic.pos < wend) {
+      fence_proxy_async_smem();
+      issue();
     }
   }
+  // never leave with copies in flight (only after a timeout can any remain)
+  if (aborted && lane == 0)
+    for (int j = k; j < issued; ++j) mbar_wait(&full[j % kScoreSlots], (j / kScoreSlots) & 1);
 }
 
 // ============================================================= select kernel
@@ -551,13 +631,16 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
 template <int D, int G>
 cudaError_t launch_score_t(const SelectArgs& a, cudaStream_t stream) {
   const asp_paged_kv& kv = *a.kv;
-  ScoreParams p{kv.summaries, a.q, kv.block_table, kv.seq_lens, a.scores, a.err,
-                kv.batch, kv.num_q_heads, kv.num_kv_heads, kv.page_size, kv.max_pages,
-                kv.num_phys_pages, 1.0f / sqrtf((float)D)};
-  dim3 grid(ceil_div(kv.max_pages, kScoreChunk), kv.batch);
-  // 16 lanes per unit while the group's queries fit in 64 registers, else 32
+  ScoreParams p{kv.summaries, a.q, kv.seq_lens, a.scores, a.err, kv.batch, kv.num_q_heads,
+                kv.num_kv_heads, kv.page_size, kv.max_pages, 1.0f / sqrtf((float)D)};
+  // 16 lanes per page while the group's queries fit in 64 registers, else 32
   constexpr int kLpu = (G * 2 * D / 16 > 64) ? 32 : 16;
-  score_kernel<D, G, kLpu><<<grid, kScoreThreads, 0, stream>>>(p);
+  const size_t smem = (size_t)kScoreWarps * kScoreSlots * (kPieceBytes + sizeof(uint64_t)) +
+                      (kv.batch + 1) * sizeof(int);
+  cudaError_t e = set_max_dynamic_smem((const void*)score_kernel<D, G, kLpu>, (int)smem);
+  if (e != cudaSuccess) return e;
+  // persistent: two CTAs per SM; the kernel splits the pages from seq_lens itself
+  score_kernel<D, G, kLpu><<<2 * a.num_sms, kScoreThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

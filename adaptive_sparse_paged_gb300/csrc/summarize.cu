@@ -7,7 +7,8 @@
 // 2*d bytes, and 16 rows are in flight per lane. bf16 min/max is exact: each
 // result is one of the inputs.
 // APPEND: one warp per (request, KV head) writes the new K/V row and folds it
-// into its page's summary.
+// into its page's summary. Summaries live in logical page order
+// [B, Hkv, max_pages, 2, d], so each segment's summaries are contiguous.
 #include "asp_internal.cuh"
 
 namespace asp {
@@ -85,7 +86,7 @@ __global__ void __launch_bounds__(256) summarize_bulk_kernel(BulkParams p) {
           mx = vmax(mx, v[t]);
         }
     }
-    V* out = reinterpret_cast<V*>(p.summ + ((size_t)phys * p.Hkv + h) * 2 * D) + lane;
+    V* out = reinterpret_cast<V*>(p.summ + (((size_t)b * p.Hkv + h) * p.max_pages + page) * 2 * D) + lane;
     out[0] = mn;     // row 0: minimum
     out[kRow] = mx;  // row 1: maximum
   }
@@ -124,7 +125,7 @@ __global__ void __launch_bounds__(256) summarize_append_kernel(AppendParams p) {
   const V vn = reinterpret_cast<const V*>(p.v_new + (size_t)unit * D)[lane];
   reinterpret_cast<V*>(p.k + (head_block * P + slot) * D)[lane] = kn;
   reinterpret_cast<V*>(p.v + (head_block * P + slot) * D)[lane] = vn;
-  V* s = reinterpret_cast<V*>(p.summ + head_block * 2 * D) + lane;
+  V* s = reinterpret_cast<V*>(p.summ + ((size_t)unit * p.max_pages + lp) * 2 * D) + lane;
   if (slot == 0) {  // a fresh page: its only token is both min and max
     s[0] = kn;
     s[kRow] = kn;

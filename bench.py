@@ -235,8 +235,7 @@ def run_asp(args):
     layers, kvs = [], []
     for l in range(w.layers):
         lay = synth.make_layer(w, sh, seed, l, dev)
-        summ = torch.empty((sh.num_phys_pages, w.num_kv_heads, 2, w.head_dim),
-                           dtype=torch.bfloat16, device=dev)
+        summ = B.new_summaries(lay.k_cache, sh.block_table)
         kv = B.PagedKV(lay.k_cache, lay.v_cache, summ, sh.block_table, sh.seq_lens, w.num_q_heads)
         layers.append(lay)
         kvs.append(kv)
@@ -286,8 +285,9 @@ def run_asp(args):
     out_bytes = Bt * Hq * d * 4 + Bt * Hq * 4
     dec_bytes = [int(lens[l].sum()) * (page_bytes + 8) + q_bytes + Bt * Hkv * 4 + out_bytes
                  for l in range(L)]                  # pages + list/table entries + q + lens + out
-    score_bytes = int(n_pages.sum()) * (Hkv * 4 * d + 4) + q_bytes   # summaries + table + q
-    select_bytes = [int(lens[l].sum()) * 4 + Bt * Hkv * 4 for l in range(L)]
+    score_bytes = int(n_pages.sum()) * Hkv * (4 * d + 4) + q_bytes  # summaries + scores + q
+    select_bytes = [int(n_pages.sum()) * Hkv * 4 + int(lens[l].sum()) * 4 + Bt * Hkv * 4
+                    for l in range(L)]                # scores + lists + lens
     step_bytes = sum(dec_bytes) + L * score_bytes + sum(select_bytes)
 
     # per-kernel durations: eager pass with events on the launching stream
@@ -383,7 +383,7 @@ def run_asp(args):
                 "gamma": args.gamma,
                 "l2": "inputs larger than L2 (K/V %.1f GiB, summaries %.2f GiB resident); no flush"
                       % (2 * sh.num_phys_pages * Hkv * P * d * 2 * L / 2**30,
-                         sh.num_phys_pages * Hkv * 4 * d * L / 2**30),
+                         Bt * Hkv * sh.max_pages * 4 * d * L / 2**30),
                 "parallelism": f"replica per GPU x{world} (requests shard, no collective)",
                 "setup_s": round(gen_s, 1),
             },

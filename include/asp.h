@@ -75,10 +75,14 @@ typedef void* asp_stream;
  *   k_cache, v_cache : bf16 [num_phys_pages, Hkv, P, d]. The (page, head) block
  *                      of P*d values is contiguous. Only asp_page_summarize in
  *                      APPEND mode writes them.
- *   summaries        : bf16 [num_phys_pages, Hkv, 2, d]; row 0 is the channel
+ *   summaries        : bf16 [batch, Hkv, max_pages, 2, d], in LOGICAL page
+ *                      order: entry (b, h, p) summarises logical page p < N_b
+ *                      of request b for KV head h; row 0 is the channel
  *                      minimum of K over the page's valid tokens, row 1 the
- *                      maximum. Written by asp_page_summarize, read by
- *                      asp_coverage_select.
+ *                      maximum. Each (request, KV head) segment's summaries
+ *                      are one contiguous run, so the estimate pass streams
+ *                      them sequentially. Written by asp_page_summarize, read
+ *                      by asp_coverage_select.
  *   block_table      : int32 [batch, max_pages]; entry (b, p) is the physical
  *                      page holding logical page p of request b. Shared by all
  *                      heads and layers. Only entries p < N_b are read.
@@ -99,7 +103,7 @@ typedef struct asp_paged_kv {
   int32_t head_dim;       /* d */
   int32_t page_size;      /* P (tokens per page) */
   int32_t max_pages;      /* columns of block_table and of the page lists */
-  int32_t num_phys_pages; /* rows of k_cache / v_cache / summaries */
+  int32_t num_phys_pages; /* rows of k_cache / v_cache */
 } asp_paged_kv;
 
 /* Library ABI version (ASP_ABI_VERSION of the build). */
@@ -113,13 +117,15 @@ const char* asp_status_string(asp_status status);
  * asp_page_summarize for this shape on the CURRENT device (the decode grid
  * is sized from its SM count). Writes the size to *bytes. The workspace is a
  * caller-owned device buffer, 256-byte aligned, that must be zeroed once with
- * asp_workspace_init before first use; after that every call leaves it ready
- * for the next (its counters return to zero), including under graph replay.
- * Calls that share one workspace must be ordered on one stream.
+ * asp_workspace_init before first use. It holds the device error word and
+ * per-call scratch (page scores, the decode's partial results and merge
+ * table) that every call rewrites before reading, so no call depends on what
+ * an earlier one left and graph replay is safe. Calls that share one
+ * workspace must be ordered on one stream.
  */
 asp_status asp_workspace_size(const asp_paged_kv* kv, size_t* bytes);
 
-/* Zeroes the workspace's error word and counters (async on `stream`). */
+/* Zeroes the whole workspace, device error word included (async on `stream`). */
 asp_status asp_workspace_init(void* ws, size_t ws_bytes, asp_stream stream);
 
 /*
@@ -128,13 +134,13 @@ asp_status asp_workspace_init(void* ws, size_t ws_bytes, asp_stream stream);
  * rule (MOIRA abstract; Quest as named in the HiSparse abstract).
  *
  * mode ASP_SUMMARIZE_BULK (0): for every request b and logical page p < N_b,
- *   recompute summaries[block_table[b,p], h] from the page's valid tokens
- *   (positions < T_b). k_new / v_new must be NULL.
+ *   recompute summaries[b, h, p] from the valid tokens (positions < T_b) of
+ *   physical page block_table[b, p]. k_new / v_new must be NULL.
  * mode ASP_SUMMARIZE_APPEND (1): seq_lens already count one new token per
  *   request (T_b >= 1). Writes k_new[b,h,:] / v_new[b,h,:] (bf16 [B, Hkv, d])
  *   into slot (T_b-1) % P of page (T_b-1) / P of k_cache / v_cache, and folds
- *   the new key into that page's summary (a fresh page, slot 0, takes the key
- *   as both its min and max). Idempotent, so replaying it is safe.
+ *   the new key into summaries[b, h, (T_b-1) / P] (a fresh page, slot 0, takes
+ *   the key as both its min and max). Idempotent, so replaying it is safe.
  * Requests with T_b == 0 are skipped. Out-of-range table entries set
  * ASP_DEVERR_PAGE_RANGE and skip the page.
  */
@@ -163,6 +169,8 @@ asp_status asp_page_summarize(const asp_paged_kv* kv, int32_t mode,
  *          page ids in ascending order; entries past lens[b,h] are untouched.
  * lens   : int32 [B, Hkv] out; the kept count (0 only when T_b == 0).
  * Masses are summed in 64-bit fixed point, so the result is deterministic.
+ * Reads summaries, seq_lens and q only (not block_table or the K/V pages):
+ * run asp_page_summarize after any change to the cache first.
  */
 asp_status asp_coverage_select(const asp_paged_kv* kv, const float* q, float gamma,
                                int32_t budget, int32_t* lists, int32_t* lens,
@@ -177,9 +185,12 @@ asp_status asp_coverage_select(const asp_paged_kv* kv, const float* q, float gam
  * valid tokens of the listed pages:
  *   out[b,h,:] = sum_t softmax_t(sm_scale * q[b,h].k_t) v_t
  *   lse[b,h]   = log sum_t exp(sm_scale * q[b,h].k_t)
- * The grid is a fixed number of CTAs; each loads the lengths, splits the
- * concatenated lists evenly, attends over its slice and merges partial
- * results by log-sum-exp. A segment with lens 0 gets out = 0, lse = -inf.
+ * The grid is a fixed number of CTAs (one per SM); each loads the lengths,
+ * splits the concatenated lists evenly and attends over its slice. A CTA
+ * whose slice holds a whole segment writes out/lse itself; otherwise it
+ * leaves a partial (max, sum, unnormalised output) in the workspace, and a
+ * second kernel, enqueued by the same call, combines a segment's partials by
+ * log-sum-exp. A segment with lens 0 gets out = 0, lse = -inf.
  * K/V are bf16; the products run on tensor cores with fp32 accumulation and
  * the probabilities are rounded to bf16 for the P.V product.
  * lists, lens : as written by asp_coverage_select (any order within a list).

@@ -34,8 +34,7 @@ class Case:
         self.layers, self.kvs = [], []
         for l in self.layer_ids:
             lay = synth.make_layer(w, self.sh, seed, l, device)
-            summ = torch.zeros((self.sh.num_phys_pages, w.num_kv_heads, 2, w.head_dim),
-                               dtype=torch.bfloat16, device=device)
+            summ = B.new_summaries(lay.k_cache, self.sh.block_table)
             kv = B.PagedKV(lay.k_cache, lay.v_cache, summ, self.sh.block_table, self.sh.seq_lens,
                            w.num_q_heads)
             self.layers.append(lay)
@@ -82,9 +81,8 @@ def check_case(case: Case, i, gamma, budget, lists, lens, out, lse, segs=None, s
         qg = q_c[b, h * g:(h + 1) * g]
         ref = O.decode_segment(qg, kp, vp, T, gamma, budget, 1.0 / math.sqrt(w.head_dim))
         if check_summaries and n:
-            idx = sh.block_table[b, :n].to(torch.long)
-            gmn = parity.bf16_np(summ[idx, h, 0])
-            gmx = parity.bf16_np(summ[idx, h, 1])
+            gmn = parity.bf16_np(summ[b, h, :n, 0])
+            gmx = parity.bf16_np(summ[b, h, :n, 1])
             assert np.array_equal(gmn, ref["mn"]) and np.array_equal(gmx, ref["mx"]), \
                 f"summaries differ at segment {(b, h)}"
         k = int(lens_c[b, h])
@@ -269,9 +267,8 @@ def test_append_matches_oracle(cuda_device):
     assert np.array_equal(parity.bf16_np(kv.v_cache), v_ref)
     summ = parity.bf16_np(kv.summaries)
     for (b, h), (mn, mx) in want.items():
-        T = lens0[b] + 1
-        phys = bt[b, (T - 1) // P]
-        assert np.array_equal(summ[phys, h, 0], mn) and np.array_equal(summ[phys, h, 1], mx)
+        lp = lens0[b] // P  # logical page of the appended token
+        assert np.array_equal(summ[b, h, lp, 0], mn) and np.array_equal(summ[b, h, lp, 1], mx)
     # after the append the whole step still matches the oracle
     res = case.run(0, 0.9)
     check_case(case, 0, 0.9, 0, *res)

@@ -25,9 +25,8 @@ def _case(dev, seed):
     w = synth.Workload("noalloc", 3, 2, 16, 4, 128, 16, seq_len=1)
     sh = synth.make_shared(w, seed, dev, seq_lens=[16 * 300 + 7, 16 * 41, 5], max_pages=320)
     layers = [synth.make_layer(w, sh, seed, l, dev) for l in range(2)]
-    summ = torch.zeros((sh.num_phys_pages, w.num_kv_heads, 2, w.head_dim), dtype=torch.bfloat16,
-                       device=dev)
-    kvs = [B.PagedKV(lay.k_cache, lay.v_cache, summ.clone(), sh.block_table, sh.seq_lens,
+    kvs = [B.PagedKV(lay.k_cache, lay.v_cache, B.new_summaries(lay.k_cache, sh.block_table),
+                     sh.block_table, sh.seq_lens,
                      w.num_q_heads) for lay in layers]
     ws = B.new_workspace(kvs[0])
     for kv in kvs:
