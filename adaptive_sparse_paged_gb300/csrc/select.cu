@@ -5,19 +5,19 @@
 // score_kernel   HBM-bound stream over the page summaries, which are kept in
 //                logical page order per (request, KV head) segment. Every
 //                warp of a persistent grid streams its own even slice of all
-//                segments' pages with 4 KiB bulk copies into a private
-//                3-slot ring. 16 lanes (32 when the group's queries would
-//                not fit in registers) score one page. A lane holds channels
-//                of either the min row or the max row, together with the
-//                matching sign part of the group's queries, so
+//                segments' pages in 4 KiB pieces into a private mbarrier ring
+//                (no warp waits on another). The Quest bound
 //                sum_i max(q_i*mn_i, q_i*mx_i) = sum_i q-_i*mn_i + q+_i*mx_i
-//                is one fp32 FMA per element (paired with fma.rn.f32x2). A
-//                transpose-reduce leaves each head's sum on a lane group; the
-//                group max times 1/sqrt(d) is the page score. Scores stay
-//                fp32: bf16 queries would move them by ~1e-3 and change lists.
+//                is a dense contraction of the group's queries with 2d
+//                summary channels per page, so it runs on the tensor cores
+//                (mma.sync m16n8k16, 8 pages per tile) with each fp32 query
+//                split into three bf16 terms: the dot products keep fp32
+//                precision (bf16 queries alone would move scores by ~1e-3
+//                and change lists) at a few instructions per page, which
+//                leaves the pass bound by HBM rather than by issue.
 //                (Gathering 512-byte per-(page, head) summaries scattered by
 //                the block table runs at under half the copy bandwidth;
-//                contiguous 4 KiB runs reach it.)
+//                contiguous runs reach it.)
 //
 // select_kernel  One CTA per segment. Softmax weights exp(s - max) are turned
 //                into fixed point (2^38 = weight of the top page), so every
@@ -50,75 +50,47 @@ struct ScoreParams {
   float inv_sqrt_d;
 };
 
-__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
+// Three bf16 terms whose sum is x to fp32 precision: s0 = rn(x),
+// s1 = rn(x - s0), s2 = rn(x - s0 - s1). Each residual is exact in fp32, and
+// bf16 x bf16 products are exact in fp32, so the tensor-core dot products
+// below carry the full fp32 query.
+__device__ __forceinline__ void split3_bf16(float x, float (&s)[3]) {
+  s[0] = __bfloat162float(__float2bfloat16_rn(x));
+  const float r1 = x - s[0];
+  s[1] = __bfloat162float(__float2bfloat16_rn(r1));
+  s[2] = __bfloat162float(__float2bfloat16_rn(r1 - s[1]));
 }
-__device__ __forceinline__ float2 unpack2(uint64_t v) {
-  float2 r;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
-  return r;
-}
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-// bf16x2 word -> (low element, high element) as an fp32 pair
-__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
-  return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
-
-// Sum of v[j] over the LPU lanes of a unit for each j < G, then the max over
-// j. The halving steps leave each lane with head j(lane) (bits of the lane
-// index); the final max is on every lane of the unit.
-template <int G, int LPU>
-__device__ __forceinline__ float group_bound_max(float (&v)[G], int lane) {
-#pragma unroll
-  for (int n = G, mask = LPU / 2; n > 1; n >>= 1, mask >>= 1) {
-    const bool up = (lane & mask) != 0;
-#pragma unroll
-    for (int i = 0; i < n / 2; ++i) {
-      const float send = up ? v[i] : v[i + n / 2];
-      const float keep = up ? v[i + n / 2] : v[i];
-      v[i] = keep + __shfl_xor_sync(kFull, send, mask);
-    }
-  }
-  float s = v[0];
-#pragma unroll
-  for (int mask = LPU / 2 / G; mask >= 1; mask >>= 1) s += __shfl_xor_sync(kFull, s, mask);
-#pragma unroll
-  for (int mask = LPU / G; mask <= LPU / 2; mask <<= 1)
-    s = fmaxf(s, __shfl_xor_sync(kFull, s, mask));
-  return s;
-}
-
-// One lane's slice of a page's summary.
-template <int Bytes>
-struct Chunk {
-  uint4 v[Bytes / 16];
-};
 
 // Summaries are stored per segment (request b, KV head h) in logical page
 // order, so this pass is one sequential stream with no block-table lookups.
 // The concatenated page space of all segments (segment-major) is split evenly
 // over the warps of a persistent grid. Each warp walks its slice as pieces of
-// up to kPieceBytes (whole pages of one segment); lane 0 bulk-copies every
-// piece into the warp's own ring of kScoreSlots slots, one mbarrier per slot,
-// so no warp ever waits on another. LPU lanes score one page (lanes
-// [0, LPU/2) take the min row with q-, the rest the max row with q+), 32 / LPU
-// pages per warp step.
+// up to kPieceBytes of one segment's pages; lane p bulk-copies page p of a
+// piece into the warp's own ring of slots (one mbarrier per slot, so no warp
+// ever waits on another). Pages sit at a stride of 4d + 16 bytes in shared
+// memory, which keeps the ldmatrix rows of 8 consecutive pages on distinct
+// banks.
+//
+// The score of 8 pages is one row.col mma chain: A = the group's queries,
+// one row per (split term, head), K = 2d with q- against the min row and q+
+// against the max row; B = the 8 pages' summaries (N = pages). Rows past
+// 3 * G are zero. Row r's head is r % G, and since G divides 8 a lane's rows
+// all share head (lane / 4) % G: the lane sums its rows, a butterfly over the
+// lanes of the other split terms completes each head's sum, and one over the
+// heads takes the max.
 constexpr int kPieceBytes = 4096;
-constexpr int kScoreSlots = 3;
 
-template <int D, int LPU>
+template <int D, int G>
 struct ScoreCfg {
-  static constexpr int kVals = 2 * D / LPU;  // channels per lane (one row)
-  static constexpr int kBpl = kVals * 2;     // bytes per lane per page
-  static constexpr int kPpi = 32 / LPU;      // pages per warp step
-  static constexpr int kPageBytes = 4 * D;   // min and max rows of one page
-  static constexpr int kPiecePages = kPieceBytes / kPageBytes;
+  static constexpr int kPageBytes = 4 * D;                      // min and max rows
+  static constexpr int kPiecePages = kPieceBytes / kPageBytes;  // 8 (d 128) or 16 (d 64)
+  static constexpr int kStride = kPageBytes + 16;               // padded page stride in smem
+  static constexpr int kSlotBytes = kPiecePages * kStride;
+  static constexpr int kKs = 2 * D / 16;                        // k-steps of one page
+  static constexpr int kBlocks = (3 * G + 7) / 8;               // 8-row A blocks holding data
+  static constexpr int kMt = (kBlocks + 1) / 2;                 // m16 tiles
+  static constexpr int kCtas = kBlocks > 2 ? 1 : 2;             // CTAs per SM (registers)
+  static constexpr int kSlots = kCtas == 2 ? 3 : 6;             // ring depth per warp
 };
 
 // Position in a warp's slice: segment (b, h), logical page lp, and the index
@@ -127,21 +99,22 @@ struct SegCursor {
   int b, h, lp, pos;
 };
 
-template <int D, int G, int LPU>
-__global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(ScoreParams p) {
-  using C = ScoreCfg<D, LPU>;
-  constexpr int kVals = C::kVals, kBpl = C::kBpl, kPpi = C::kPpi;
-  constexpr int kPiecePages = C::kPiecePages, kPageBytes = C::kPageBytes;
+template <int D, int G>
+__global__ void __launch_bounds__(kScoreThreads, ScoreCfg<D, G>::kCtas)
+    score_kernel(ScoreParams p) {
+  using C = ScoreCfg<D, G>;
+  constexpr int kPiecePages = C::kPiecePages, kPageBytes = C::kPageBytes, kStride = C::kStride;
+  constexpr int kSlots = C::kSlots, kKs = C::kKs, kBlocks = C::kBlocks, kMt = C::kMt;
   extern __shared__ __align__(128) uint8_t score_smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  constexpr int kRingBytes = kScoreWarps * kScoreSlots * kPieceBytes;
-  uint8_t* ring = score_smem + warp * kScoreSlots * kPieceBytes;  // this warp's slots
-  uint64_t* full = reinterpret_cast<uint64_t*>(score_smem + kRingBytes) + warp * kScoreSlots;
+  constexpr int kRingBytes = kScoreWarps * kSlots * C::kSlotBytes;
+  uint8_t* ring = score_smem + warp * kSlots * C::kSlotBytes;  // this warp's slots
+  uint64_t* full = reinterpret_cast<uint64_t*>(score_smem + kRingBytes) + warp * kSlots;
   int* rprefix = reinterpret_cast<int*>(score_smem + kRingBytes +
-                                        kScoreWarps * kScoreSlots * sizeof(uint64_t));  // [B + 1]
+                                        kScoreWarps * kSlots * sizeof(uint64_t));  // [B + 1]
 
   if (lane == 0) {
-    for (int i = 0; i < kScoreSlots; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i < kSlots; ++i) mbar_init(&full[i], 1);
     mbar_fence_init();
   }
   // prefix of the requests' page counts N_b (clamped sequence lengths)
@@ -197,47 +170,54 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(ScoreParams p) 
     }
   };
   int issued = 0;
-  auto issue = [&]() {  // next piece of the slice into slot issued % kScoreSlots
+  auto issue = [&]() {  // next piece of the slice into slot issued % kSlots
     const int n = piece_pages(ic);
-    if (lane == 0) {
-      const int slot = issued % kScoreSlots;
-      const size_t first = ((size_t)ic.b * p.Hkv + ic.h) * p.max_pages + ic.lp;
-      mbar_arrive_expect_tx(&full[slot], n * kPageBytes);
-      bulk_g2s(ring + slot * kPieceBytes,
-               reinterpret_cast<const uint8_t*>(p.summ) + first * kPageBytes, n * kPageBytes,
+    const int slot = issued % kSlots;
+    if (lane == 0) mbar_arrive_expect_tx(&full[slot], n * kPageBytes);
+    __syncwarp();
+    if (lane < n) {
+      const size_t page = ((size_t)ic.b * p.Hkv + ic.h) * p.max_pages + ic.lp + lane;
+      bulk_g2s(ring + slot * C::kSlotBytes + lane * kStride,
+               reinterpret_cast<const uint8_t*>(p.summ) + page * kPageBytes, kPageBytes,
                &full[slot]);
     }
     advance(ic, n);
     ++issued;
   };
-  for (int k = 0; k < kScoreSlots && ic.pos < wend; ++k) issue();
+  for (int k = 0; k < kSlots && ic.pos < wend; ++k) issue();
 
-  const int ul = lane % LPU, part = ul >= LPU / 2, ur = ul % (LPU / 2), pslot = lane / LPU;
-  // chunk c of this lane = bytes [(c * LPU/2 + ur) * 16, +16) of its row
-  const int lane_off = part * 2 * D + ur * 16;
-  uint64_t qv[G][kVals / 2];
+  // A operand: block bi holds rows 8 bi + lane / 4; qa[bi][ks] = the two
+  // registers of that row at k-step ks (k = 16 ks + 2 (lane % 4) + {0, 1}
+  // and the same + 8).
+  const int g = lane >> 2, t = lane & 3;
+  uint32_t qa[kBlocks][kKs][2];
   auto load_q = [&](int b, int h) {
-    const float* qp = p.q + ((size_t)b * p.Hq + h * G) * D + ur * 8;
+    const float* qp = p.q + ((size_t)b * p.Hq + h * G + g % G) * D;
 #pragma unroll
-    for (int jj = 0; jj < G; ++jj)
+    for (int ks = 0; ks < kKs; ++ks)
 #pragma unroll
-      for (int i = 0; i < kVals; i += 4) {  // chunk i/8 holds channels (i/8 * LPU/2 + ur) * 8 + [0, 8)
-        const float4 x = *reinterpret_cast<const float4*>(
-            qp + (size_t)jj * D + (i / 8) * (LPU / 2) * 8 + (i % 8));
-        const float a0 = part ? fmaxf(x.x, 0.f) : fminf(x.x, 0.f);
-        const float a1 = part ? fmaxf(x.y, 0.f) : fminf(x.y, 0.f);
-        const float a2 = part ? fmaxf(x.z, 0.f) : fminf(x.z, 0.f);
-        const float a3 = part ? fmaxf(x.w, 0.f) : fminf(x.w, 0.f);
-        qv[jj][i / 2] = pack2(a0, a1);
-        qv[jj][i / 2 + 1] = pack2(a2, a3);
+      for (int e = 0; e < 2; ++e) {
+        const int k = 16 * ks + 2 * t + 8 * e;  // k < D: q- with the min row, else q+ with max
+        const float2 x = *reinterpret_cast<const float2*>(qp + (k < D ? k : k - D));
+        float s0[3], s1[3];
+        split3_bf16(k < D ? fminf(x.x, 0.f) : fmaxf(x.x, 0.f), s0);
+        split3_bf16(k < D ? fminf(x.y, 0.f) : fmaxf(x.y, 0.f), s1);
+#pragma unroll
+        for (int bi = 0; bi < kBlocks; ++bi) {
+          const int r = 8 * bi + g, sp = r / G;  // split term of row r (>= 3: zero row)
+          const float lo = sp == 0 ? s0[0] : sp == 1 ? s0[1] : sp == 2 ? s0[2] : 0.f;
+          const float hi = sp == 0 ? s1[0] : sp == 1 ? s1[1] : sp == 2 ? s1[2] : 0.f;
+          qa[bi][ks][e] = pack_bf16(lo, hi);
+        }
       }
   };
   int qseg = -1, k = 0;
   bool aborted = false;
+  const uint32_t lane_row = (uint32_t)((lane & 7) * kStride + (lane >> 3) * 16);
 #pragma unroll 1
   for (; cc.pos < wend; ++k) {
-    const int slot = k % kScoreSlots;
-    if (!__all_sync(kFull, mbar_wait(&full[slot], (k / kScoreSlots) & 1))) {
+    const int slot = k % kSlots;
+    if (!__all_sync(kFull, mbar_wait(&full[slot], (k / kSlots) & 1))) {
       if (lane == 0) report(p.err, ASP_DEVERR_TIMEOUT);
       aborted = true;
       break;
@@ -247,31 +227,58 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(ScoreParams p) 
       load_q(cc.b, cc.h);
       qseg = seg;
     }
-    const uint8_t* sb = ring + slot * kPieceBytes + lane_off;
+    const uint32_t sb = smem_u32(ring + slot * C::kSlotBytes) + lane_row;
     float* out = p.scores + (size_t)seg * p.max_pages + cc.lp;
-#pragma unroll 2
-    for (int i0 = 0; i0 < n; i0 += kPpi) {
-      const int pg = i0 + pslot;
-      const int pr = min(pg, n - 1);  // lanes past the piece re-read its last page
-      Chunk<kBpl> x;
 #pragma unroll
-      for (int c = 0; c < kBpl / 16; ++c)
-        x.v[c] = *reinterpret_cast<const uint4*>(sb + pr * kPageBytes + c * (LPU / 2) * 16);
-      const uint32_t* w = reinterpret_cast<const uint32_t*>(&x);
-      uint64_t xv[kVals / 2];
+    for (int nt = 0; nt < kPiecePages / 8; ++nt) {
+      if (nt * 8 >= n) break;  // warp-uniform
+      float acc[kMt][2][4];    // [m tile][min half, max half][fragment]
 #pragma unroll
-      for (int m = 0; m < kVals / 2; ++m) xv[m] = bf16x2_to_f32x2(w[m]);
-      float acc[G];
+      for (int mt = 0; mt < kMt; ++mt)
 #pragma unroll
-      for (int jj = 0; jj < G; ++jj) {
-        uint64_t a2 = 0;
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
-        for (int m = 0; m < kVals / 2; ++m) a2 = ffma2(qv[jj][m], xv[m], a2);
-        const float2 f = unpack2(a2);
-        acc[jj] = f.x + f.y;
+          for (int j = 0; j < 4; ++j) acc[mt][c][j] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < kKs; ks += 2) {
+        uint32_t bf[4];  // (b0, b1) of k-step ks, then of ks + 1
+        ldsm_x4(sb + nt * 8 * kStride + ks * 32, bf);
+        constexpr int kHalfKs = kKs / 2;
+#pragma unroll
+        for (int mt = 0; mt < kMt; ++mt) {
+          const bool up = 2 * mt + 1 < kBlocks;
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const uint32_t a[4] = {qa[2 * mt][ks + u][0], up ? qa[2 * mt + up][ks + u][0] : 0u,
+                                   qa[2 * mt][ks + u][1], up ? qa[2 * mt + up][ks + u][1] : 0u};
+            mma16816(acc[mt][ks >= kHalfKs], a, bf[2 * u], bf[2 * u + 1]);
+          }
+        }
       }
-      const float sc = group_bound_max<G, LPU>(acc, lane) * p.inv_sqrt_d;
-      if (ul == 0 && pg < n) out[pg] = sc;
+      // this lane's rows share head g % G: columns 2t and 2t + 1
+      float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < kMt; ++mt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          x0 += acc[mt][c][0] + acc[mt][c][2];
+          x1 += acc[mt][c][1] + acc[mt][c][3];
+        }
+#pragma unroll
+      for (int m = 4 * G; m <= 16; m <<= 1) {  // the other split terms of the head
+        x0 += __shfl_xor_sync(kFull, x0, m);
+        x1 += __shfl_xor_sync(kFull, x1, m);
+      }
+#pragma unroll
+      for (int m = 4; m < 4 * G; m <<= 1) {  // max over the group's heads
+        x0 = fmaxf(x0, __shfl_xor_sync(kFull, x0, m));
+        x1 = fmaxf(x1, __shfl_xor_sync(kFull, x1, m));
+      }
+      const int pg = nt * 8 + 2 * t;
+      if (g == 0) {
+        if (pg < n) out[pg] = x0 * p.inv_sqrt_d;
+        if (pg + 1 < n) out[pg + 1] = x1 * p.inv_sqrt_d;
+      }
     }
     advance(cc, n);
     __syncwarp();  // every lane is done reading the slot
@@ -282,7 +289,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(ScoreParams p) 
   }
   // never leave with copies in flight (only after a timeout can any remain)
   if (aborted && lane == 0)
-    for (int j = k; j < issued; ++j) mbar_wait(&full[j % kScoreSlots], (j / kScoreSlots) & 1);
+    for (int j = k; j < issued; ++j) mbar_wait(&full[j % kSlots], (j / kSlots) & 1);
 }
 
 // ============================================================= select kernel
@@ -633,14 +640,13 @@ cudaError_t launch_score_t(const SelectArgs& a, cudaStream_t stream) {
   const asp_paged_kv& kv = *a.kv;
   ScoreParams p{kv.summaries, a.q, kv.seq_lens, a.scores, a.err, kv.batch, kv.num_q_heads,
                 kv.num_kv_heads, kv.page_size, kv.max_pages, 1.0f / sqrtf((float)D)};
-  // 16 lanes per page while the group's queries fit in 64 registers, else 32
-  constexpr int kLpu = (G * 2 * D / 16 > 64) ? 32 : 16;
-  const size_t smem = (size_t)kScoreWarps * kScoreSlots * (kPieceBytes + sizeof(uint64_t)) +
+  using C = ScoreCfg<D, G>;
+  const size_t smem = (size_t)kScoreWarps * C::kSlots * (C::kSlotBytes + sizeof(uint64_t)) +
                       (kv.batch + 1) * sizeof(int);
-  cudaError_t e = set_max_dynamic_smem((const void*)score_kernel<D, G, kLpu>, (int)smem);
+  cudaError_t e = set_max_dynamic_smem((const void*)score_kernel<D, G>, (int)smem);
   if (e != cudaSuccess) return e;
-  // persistent: two CTAs per SM; the kernel splits the pages from seq_lens itself
-  score_kernel<D, G, kLpu><<<2 * a.num_sms, kScoreThreads, smem, stream>>>(p);
+  // persistent: the kernel splits the pages it finds in seq_lens itself
+  score_kernel<D, G><<<C::kCtas * a.num_sms, kScoreThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
