@@ -77,6 +77,11 @@ cudaError_t set_max_dynamic_smem(const void* func, int bytes) {
     if (done_func[i] == func && done_dev[i] == dev && done_bytes[i] >= bytes) return cudaSuccess;
   e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
+  // Every kernel of the library asks for the largest shared-memory carveout,
+  // so consecutive kernels never make an SM flush L1 and repartition it.
+  e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
   if (n_done < 256) {
     done_func[n_done] = func;
     done_dev[n_done] = dev;

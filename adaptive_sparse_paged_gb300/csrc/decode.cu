@@ -486,54 +486,58 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 // are combined in CTA order, so the result does not depend on timing.
 struct MergeParams {
   const float* partials;
-  const int32_t* table;
+  const int32_t* merge_table;
   float* out;
   float* lse;
   int Hq, Hkv, g, D, slot_floats;
 };
 
+// One CTA per split segment, one thread per output element (query head col,
+// channel d). After the merge-table entry every load is independent: a thread
+// reads each piece's (m, l) for its head (the same words across a warp, since
+// a warp never spans two heads) and its own element of each piece's output,
+// and folds them in with an online log-sum-exp in the log2 domain.
 __global__ void __launch_bounds__(1024) merge_kernel(const MergeParams p) {
-  extern __shared__ float ms[];  // [np][8] weights, [np][8] l, M[8], L[8]
-  const int s = blockIdx.x, tid = threadIdx.x;
-  const int t = p.table[s];
+  const int s = blockIdx.x, tid = threadIdx.x, D = p.D;
+  const int t = p.merge_table[s];
   const int cf = t >> 16, cl = t & 0xffff;
-  if (cf >= cl) return;
+  if (cf >= cl || tid >= p.g * D) return;
+  const int col = tid / D, d = tid % D;
+  const float* base = p.partials + (size_t)(s + cf) * p.slot_floats;
   const int np = cl - cf + 1;
-  float* wm = ms;
-  float* wl = ms + np * 8;
-  float* ml = ms + np * 16;
-  for (int e = tid; e < np * 8; e += blockDim.x) {
-    const float* q = p.partials + (size_t)(s + cf + e / 8) * p.slot_floats;
-    wm[e] = q[e % 8];
-    wl[e] = q[8 + (e % 8)];
-  }
-  __syncthreads();
-  if (tid < p.g) {
-    float M = -INFINITY;
-    for (int c = 0; c < np; ++c) M = fmaxf(M, wm[c * 8 + tid]);
-    float L = 0.f;
-    for (int c = 0; c < np; ++c) {
-      const float w = M == -INFINITY ? 0.f : exp2f(wm[c * 8 + tid] - M);
-      wm[c * 8 + tid] = w;
-      L += w * wl[c * 8 + tid];
+  float M = -INFINITY, L = 0.f, acc = 0.f;
+  auto fold = [&](float m, float l, float o) {
+    if (m == -INFINITY) return;  // a piece with no valid token
+    if (m > M) {
+      const float sc = exp2f(M - m);  // 0 while M is still -inf
+      acc *= sc;
+      L *= sc;
+      M = m;
     }
-    ml[tid] = M;
-    ml[8 + tid] = L;
+    const float w = exp2f(m - M);
+    acc += w * o;
+    L += w * l;
+  };
+  constexpr int kU = 8;  // pieces whose loads are in flight together
+  for (int c = 0; c < np; c += kU) {
+    float m[kU], l[kU], o[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      m[u] = -INFINITY;
+      if (c + u < np) {
+        const float* q = base + (size_t)(c + u) * p.slot_floats;
+        m[u] = q[col];
+        l[u] = q[8 + col];
+        o[u] = q[16 + col * D + d];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) fold(m[u], l[u], o[u]);
   }
-  __syncthreads();
-  // one thread per output element; the piece loads are independent
-  const int b = s / p.Hkv, h = s % p.Hkv, D = p.D;
-  if (tid < p.g * D) {
-    const int col = tid / D, d = tid % D;
-    const float* src = p.partials + (size_t)(s + cf) * p.slot_floats + 16 + col * D + d;
-    float acc = 0.f;
-#pragma unroll 16
-    for (int c = 0; c < np; ++c) acc += wm[c * 8 + col] * src[(size_t)c * p.slot_floats];
-    const float M = ml[col], L = ml[8 + col];
-    const size_t row = (size_t)b * p.Hq + h * p.g + col;
-    p.out[row * D + d] = L > 0.f ? acc / L : 0.f;
-    if (d == 0) p.lse[row] = L > 0.f ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
-  }
+  const int b = s / p.Hkv, h = s % p.Hkv;
+  const size_t row = (size_t)b * p.Hq + h * p.g + col;
+  p.out[row * D + d] = L > 0.f ? acc / L : 0.f;
+  if (d == 0) p.lse[row] = L > 0.f ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
 }
 
 // ----------------------------------------------------------------- host side
@@ -586,9 +590,8 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   MergeParams mp{a.partials, a.merge_table, a.out, a.lse, kv.num_q_heads, kv.num_kv_heads,
                  kv.num_q_heads / kv.num_kv_heads, D, a.slot_floats};
-  const size_t msmem = ((size_t)a.grid * 16 + 16) * sizeof(float);
-  if ((e = set_max_dynamic_smem((const void*)merge_kernel, (int)msmem)) != cudaSuccess) return e;
-  merge_kernel<<<S, (kv.num_q_heads / kv.num_kv_heads) * D, msmem, stream>>>(mp);
+  if ((e = set_max_dynamic_smem((const void*)merge_kernel, 0)) != cudaSuccess) return e;
+  merge_kernel<<<S, (kv.num_q_heads / kv.num_kv_heads) * D, 0, stream>>>(mp);
   return cudaGetLastError();
 }
 

@@ -295,10 +295,13 @@ __global__ void __launch_bounds__(kScoreThreads, ScoreCfg<D, G>::kCtas)
 // ============================================================= select kernel
 constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kSelCache = 8192;  // scores cached in shared memory when N fits
+constexpr int kSelCache = 8192;  // N up to this: the fast path (scores in registers and smem)
+constexpr int kPer = kSelCache / kSelThreads;  // elements per thread on the fast path
 constexpr int kBins = 256;
 constexpr int kLimbBits = 13;    // mass = l0 + l1 << 13 + l2 << 26, each limb < 2^13
 constexpr int kWarpCand = 4096;  // candidates one warp finishes on (fits the histogram area)
+constexpr int kLinBins = 4096;   // bins of the first, linear round
+constexpr int kLinLoBits = 19;   // fast path: a weight is lo + hi << 19, both < 2^19
 constexpr size_t kSelSmem = (size_t)kSelWarps * kBins * 4 * sizeof(uint32_t) +  // private hists
                             kSelCache * sizeof(float);                            // score cache
 
@@ -322,9 +325,11 @@ __device__ __forceinline__ uint32_t score_key(float s) {
 __device__ __forceinline__ float key_score(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
-// Softmax weight of a page relative to the top page, in 2^-38 units (<= 2^38).
+// Softmax weight of a page relative to the top page, in 2^-37 units
+// (<= 2^37, so 8192 of them sum below 2^50 and the fast path's 19-bit limbs
+// sum below 2^32).
 __device__ __forceinline__ unsigned long long mass_fixed(float s, float smax) {
-  return __float2ull_rn(expf(s - smax) * 274877906944.0f);
+  return __float2ull_rn(expf(s - smax) * 137438953472.0f);
 }
 
 template <typename T>
@@ -352,6 +357,29 @@ __device__ __forceinline__ T block_reduce(T v, T* scratch, int op /*0 sum, 1 min
   return r;
 }
 
+// Block min and max of one float pair in a single pass (scratch: 2 x warps).
+__device__ __forceinline__ void block_minmax(float& mn, float& mx, float* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(kFull, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+  }
+  if (lane == 0) {
+    scratch[warp] = mn;
+    scratch[kSelWarps + warp] = mx;
+  }
+  __syncthreads();
+  mn = scratch[lane];
+  mx = scratch[kSelWarps + lane];
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(kFull, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+  }
+  __syncthreads();  // scratch is free again
+}
+
 __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
   extern __shared__ __align__(16) uint8_t sel_smem[];
   uint32_t* hist = reinterpret_cast<uint32_t*>(sel_smem);  // [warp][bin][count, l0, l1, l2]
@@ -359,9 +387,11 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
   __shared__ uint32_t m_cnt[kBins];
   __shared__ unsigned long long m_mass[kBins];
   __shared__ unsigned long long red_u64[kSelWarps];
-  __shared__ float red_f[kSelWarps];
+  __shared__ uint32_t red_u32[2 * kSelWarps];
+  __shared__ float red_f[2 * kSelWarps];
   __shared__ uint32_t pick[4];
   __shared__ unsigned long long pick_m[1];
+  __shared__ uint32_t slab_cnt[kPer * kSelWarps][2];  // fast compaction: (gt, eq) per (slab, warp)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int s = blockIdx.x;
@@ -380,36 +410,171 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
     return;
   }
   const float* gsc = p.scores + (size_t)s * p.max_pages;
-  const bool cached = N <= kSelCache;
+  // fast path: element k of this thread is page id k * kSelThreads + tid, so a
+  // warp's elements of one slab k are 32 consecutive ids
+  const bool fast = N <= kSelCache;
+  float v[kPer];
   float lo_s = INFINITY, hi_s = -INFINITY;
-  for (int i = tid; i < N; i += kSelThreads) {
-    const float v = gsc[i];
-    if (cached) cache[i] = v;
-    lo_s = fminf(lo_s, v);
-    hi_s = fmaxf(hi_s, v);
-  }
-  lo_s = block_reduce<float>(lo_s, red_f, 1);
-  hi_s = block_reduce<float>(hi_s, red_f, 2);
-  const float* sc = cached ? cache : gsc;
-  const float smax = hi_s;
-
-  unsigned long long target;
-  if (mass_mode) {
-    unsigned long long z = 0;
-    for (int i = tid; i < N; i += kSelThreads) z += mass_fixed(sc[i], smax);
-    z = block_reduce<unsigned long long>(z, red_u64, 0);
-    target = (unsigned long long)ceil((double)p.gamma * (double)z);
-    if (target < 1) target = 1;
+  if (fast) {
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = k * kSelThreads + tid;
+      v[k] = -INFINITY;
+      if (i < N) {
+        v[k] = gsc[i];
+        cache[i] = v[k];
+        lo_s = fminf(lo_s, v[k]);
+        hi_s = fmaxf(hi_s, v[k]);
+      }
+    }
   } else {
-    target = (unsigned long long)p.budget;
+    for (int i = tid; i < N; i += kSelThreads) {
+      const float x = gsc[i];
+      lo_s = fminf(lo_s, x);
+      hi_s = fmaxf(hi_s, x);
+    }
+  }
+  block_minmax(lo_s, hi_s, red_f);
+  const float* sc = fast ? cache : gsc;
+  const float smax = hi_s;
+  auto weight = [&](float x) -> unsigned long long { return mass_mode ? mass_fixed(x, smax) : 1ull; };
+
+  // selection weights (fixed-point softmax mass, or 1 in budget mode) and target
+  unsigned long long mw[kPer];
+  unsigned long long target;
+  {
+    unsigned long long z = 0;
+    if (fast) {
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        mw[k] = k * kSelThreads + tid < N ? weight(v[k]) : 0ull;
+        z += mw[k];
+      }
+    } else if (mass_mode) {
+      for (int i = tid; i < N; i += kSelThreads) z += mass_fixed(sc[i], smax);
+    }
+    if (mass_mode) {
+      z = block_reduce<unsigned long long>(z, red_u64, 0);
+      target = (unsigned long long)ceil((double)p.gamma * (double)z);
+      if (target < 1) target = 1;
+    } else {
+      target = (unsigned long long)p.budget;
+    }
   }
 
-  // radix select of the cutoff key over the candidates' key range
-  uint32_t lo = score_key(lo_s), hi = score_key(hi_s);
+  // state of the cutoff search: candidates are the keys in [lo, hi]; above_m
+  // (above_c) is the weight (count) of every element with a larger key
+  uint32_t lo = 0, hi = 0;
   unsigned long long above_m = 0;
   uint32_t above_c = 0, cnt_eq = 0;
   uint32_t* my_hist = hist + warp * kBins * 4;
   constexpr uint32_t kLimbMask = (1u << kLimbBits) - 1u;
+
+  // Round 1: one histogram of bins linear in the distance from the top score,
+  // smax - s, over at most 28 units in mass mode (a page further down has
+  // zero fixed-point mass). The bin index never increases with the score, so
+  // the bin where the running weight from the top reaches the target holds
+  // one interval of keys, usually a handful.
+  const float span = mass_mode ? fminf(hi_s - lo_s, 28.f) : hi_s - lo_s;
+  const float inv_w = span > 0.f ? (float)kLinBins / span : 0.f;
+  auto lin_bin = [&](float x) { return min(kLinBins - 1, (int)((smax - x) * inv_w)); };
+  int jbin;
+  {
+    uint32_t* lin_lo = hist;             // fast: weight limbs; general: count
+    uint32_t* lin_hi = hist + kLinBins;  // fast: weight limbs
+    unsigned long long* lin_w = reinterpret_cast<unsigned long long*>(hist + kLinBins);  // general
+    const int words = fast ? 2 * kLinBins : 3 * kLinBins;
+    for (int i = tid; i < words / 4; i += kSelThreads)
+      reinterpret_cast<uint4*>(hist)[i] = make_uint4(0, 0, 0, 0);
+    if (tid == 0) pick[3] = 0;  // candidate counter of the fast path
+    __syncthreads();
+    if (fast) {
+#pragma unroll
+      for (int k = 0; k < kPer; ++k)
+        if (mw[k]) {
+          const int bin = lin_bin(v[k]);
+          atomicAdd(&lin_lo[bin], (uint32_t)mw[k] & ((1u << kLinLoBits) - 1u));
+          const uint32_t h = (uint32_t)(mw[k] >> kLinLoBits);
+          if (h) atomicAdd(&lin_hi[bin], h);
+        }
+    } else {
+      for (int i = tid; i < N; i += kSelThreads) {
+        const float x = sc[i];
+        const int bin = lin_bin(x);
+        atomicAdd(&lin_lo[bin], 1u);
+        atomicAdd(&lin_w[bin], weight(x));
+      }
+    }
+    __syncthreads();
+    // block scan over the bins; thread tid owns bins [kPb tid, kPb tid + kPb)
+    constexpr int kPb = kLinBins / kSelThreads;
+    unsigned long long w[kPb], ws = 0;
+    uint32_t c[kPb], cs = 0;
+#pragma unroll
+    for (int u = 0; u < kPb; ++u) {
+      const int bin = tid * kPb + u;
+      w[u] = fast ? lin_lo[bin] + ((unsigned long long)lin_hi[bin] << kLinLoBits) : lin_w[bin];
+      c[u] = fast ? 0u : lin_lo[bin];
+      ws += w[u];
+      cs += c[u];
+    }
+    unsigned long long xw = ws;
+    uint32_t xc = cs;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long yw = __shfl_up_sync(kFull, xw, o);
+      const uint32_t yc = __shfl_up_sync(kFull, xc, o);
+      if (lane >= o) {
+        xw += yw;
+        xc += yc;
+      }
+    }
+    if (lane == 31) {
+      red_u64[warp] = xw;
+      red_u32[warp] = xc;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const unsigned long long w0 = red_u64[lane];
+      const uint32_t c0 = red_u32[lane];
+      unsigned long long aw = w0;
+      uint32_t ac = c0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long yw = __shfl_up_sync(kFull, aw, o);
+        const uint32_t yc = __shfl_up_sync(kFull, ac, o);
+        if (lane >= o) {
+          aw += yw;
+          ac += yc;
+        }
+      }
+      red_u64[lane] = aw - w0;  // exclusive warp offsets
+      red_u32[lane] = ac - c0;
+    }
+    __syncthreads();
+    unsigned long long run_w = red_u64[warp] + xw - ws;
+    uint32_t run_c = red_u32[warp] + xc - cs;
+    // exactly one bin has run_w < target <= run_w + w (target <= total weight)
+#pragma unroll
+    for (int u = 0; u < kPb; ++u) {
+      if (run_w < target && run_w + w[u] >= target) {
+        pick[0] = (uint32_t)(tid * kPb + u);
+        pick[1] = run_c;
+        pick[2] = c[u];
+        pick_m[0] = run_w;
+      }
+      run_w += w[u];
+      run_c += c[u];
+    }
+    __syncthreads();
+    jbin = (int)pick[0];
+    above_m = pick_m[0];
+    // counts are tracked only where the weight is not already a count
+    above_c = fast ? (mass_mode ? 0u : (uint32_t)above_m) : pick[1];
+    cnt_eq = pick[2];
+    __syncthreads();  // pick[0..2] are rewritten below
+  }
+
   // warp 0: lane owns bins [8*lane, 8*lane+8) of m_cnt/m_mass; finds the
   // largest bin j with above + (sum over bins >= j) >= target
   auto pick_bin = [&]() {
@@ -472,124 +637,298 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
     const int bits = range ? 32 - __clz(range) : 0;
     return bits > 8 ? bits - 8 : 0;
   };
-
-  // Block-wide rounds over every element while the picked bin is large.
-  bool resolved = false;
-  while (true) {
-    const int shift = shift_of();
-    for (int i = tid; i < kSelWarps * kBins; i += kSelThreads)
-      reinterpret_cast<uint4*>(hist)[i] = make_uint4(0, 0, 0, 0);
-    __syncthreads();
-    for (int i = tid; i < N; i += kSelThreads) {
-      const float v = sc[i];
-      const uint32_t k = score_key(v);
-      if (k >= lo && k <= hi) {
-        uint32_t* h = my_hist + ((k - lo) >> shift) * 4;
-        atomicAdd(h, 1u);
-        if (mass_mode) {
-          const unsigned long long m = mass_fixed(v, smax);
-          atomicAdd(h + 1, (uint32_t)m & kLimbMask);
-          atomicAdd(h + 2, (uint32_t)(m >> kLimbBits) & kLimbMask);
-          atomicAdd(h + 3, (uint32_t)(m >> (2 * kLimbBits)));
-        }
-      }
-    }
-    __syncthreads();
-    if (tid < kBins) {  // merge the private histograms of bin tid
-      uint32_t c = 0;
-      unsigned long long l0 = 0, l1 = 0, l2 = 0;
-      for (int w = 0; w < kSelWarps; ++w) {
-        const uint4 h = reinterpret_cast<const uint4*>(hist)[w * kBins + tid];
-        c += h.x;
-        l0 += h.y;
-        l1 += h.z;
-        l2 += h.w;
-      }
-      m_cnt[tid] = c;
-      m_mass[tid] = l0 + (l1 << kLimbBits) + (l2 << (2 * kLimbBits));
-    }
-    __syncthreads();
-    if (warp == 0) pick_bin();
-    __syncthreads();
-    narrow(shift);
-    if (shift == 0) {
-      resolved = true;
-      break;
-    }
-    if (cnt_eq <= kWarpCand) break;  // few candidates left: one warp finishes
-    __syncthreads();
-  }
-  if (!resolved) {
-    // gather the candidates (scores with keys in [lo, hi]) and let warp 0
-    // run the remaining rounds on them with warp-level synchronisation only
-    float* cand = reinterpret_cast<float*>(hist + kBins * 4);  // after warp 0's histogram
-    if (tid == 0) pick[3] = 0;
-    __syncthreads();
-    for (int i = tid; i < N; i += kSelThreads) {
-      const float v = sc[i];
-      const uint32_t k = score_key(v);
-      if (k >= lo && k <= hi) cand[atomicAdd(&pick[3], 1u)] = v;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      const int nc = (int)pick[3];
-      while (true) {
-        const int shift = shift_of();
-        for (int i = lane; i < kBins; i += 32)
-          reinterpret_cast<uint4*>(hist)[i] = make_uint4(0, 0, 0, 0);
-        __syncwarp();
-        for (int i = lane; i < nc; i += 32) {
-          const float v = cand[i];
-          const uint32_t k = score_key(v);
-          if (k >= lo && k <= hi) {
-            uint32_t* h = hist + ((k - lo) >> shift) * 4;
-            atomicAdd(h, 1u);
-            if (mass_mode) {
-              const unsigned long long m = mass_fixed(v, smax);
-              atomicAdd(h + 1, (uint32_t)m & kLimbMask);
-              atomicAdd(h + 2, (uint32_t)(m >> kLimbBits) & kLimbMask);
-              atomicAdd(h + 3, (uint32_t)(m >> (2 * kLimbBits)));
-            }
+  // Exact radix rounds on the keys in [lo, hi] until one key is left: block
+  // rounds over every element while more than kWarpCand remain, then warp 0
+  // alone on the gathered candidates. Leaves the cutoff key in lo.
+  auto radix_resolve = [&]() {
+    bool resolved = lo == hi;
+    while (!resolved && cnt_eq > kWarpCand) {
+      const int shift = shift_of();
+      for (int i = tid; i < kSelWarps * kBins; i += kSelThreads)
+        reinterpret_cast<uint4*>(hist)[i] = make_uint4(0, 0, 0, 0);
+      __syncthreads();
+      for (int i = tid; i < N; i += kSelThreads) {
+        const float x = sc[i];
+        const uint32_t k = score_key(x);
+        if (k >= lo && k <= hi) {
+          uint32_t* h = my_hist + ((k - lo) >> shift) * 4;
+          atomicAdd(h, 1u);
+          if (mass_mode) {
+            const unsigned long long m = mass_fixed(x, smax);
+            atomicAdd(h + 1, (uint32_t)m & kLimbMask);
+            atomicAdd(h + 2, (uint32_t)(m >> kLimbBits) & kLimbMask);
+            atomicAdd(h + 3, (uint32_t)(m >> (2 * kLimbBits)));
           }
         }
-        __syncwarp();
-        for (int i = lane; i < kBins; i += 32) {
-          const uint4 h = reinterpret_cast<const uint4*>(hist)[i];
-          m_cnt[i] = h.x;
-          m_mass[i] = (unsigned long long)h.y + ((unsigned long long)h.z << kLimbBits) +
-                      ((unsigned long long)h.w << (2 * kLimbBits));
-        }
-        __syncwarp();
-        pick_bin();
-        __syncwarp();
-        narrow(shift);
-        __syncwarp();
-        if (shift == 0) break;
       }
-      if (lane == 0) {  // publish the result for the whole block
-        pick[0] = lo;
-        pick[1] = above_c;
-        pick[2] = cnt_eq;
-        pick_m[0] = above_m;
+      __syncthreads();
+      if (tid < kBins) {  // merge the private histograms of bin tid
+        uint32_t c = 0;
+        unsigned long long l0 = 0, l1 = 0, l2 = 0;
+        for (int w = 0; w < kSelWarps; ++w) {
+          const uint4 h = reinterpret_cast<const uint4*>(hist)[w * kBins + tid];
+          c += h.x;
+          l0 += h.y;
+          l1 += h.z;
+          l2 += h.w;
+        }
+        m_cnt[tid] = c;
+        m_mass[tid] = l0 + (l1 << kLimbBits) + (l2 << (2 * kLimbBits));
+      }
+      __syncthreads();
+      if (warp == 0) pick_bin();
+      __syncthreads();
+      narrow(shift);
+      resolved = shift == 0;
+      __syncthreads();
+    }
+    if (!resolved) {
+      // gather the candidates (scores with keys in [lo, hi]) and let warp 0
+      // run the remaining rounds on them with warp-level synchronisation only
+      float* cand = reinterpret_cast<float*>(hist + kBins * 4);  // after warp 0's histogram
+      if (tid == 0) pick[3] = 0;
+      __syncthreads();
+      for (int i = tid; i < N; i += kSelThreads) {
+        const float x = sc[i];
+        const uint32_t k = score_key(x);
+        if (k >= lo && k <= hi) cand[atomicAdd(&pick[3], 1u)] = x;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        const int nc = (int)pick[3];
+        while (true) {
+          const int shift = shift_of();
+          for (int i = lane; i < kBins; i += 32)
+            reinterpret_cast<uint4*>(hist)[i] = make_uint4(0, 0, 0, 0);
+          __syncwarp();
+          for (int i = lane; i < nc; i += 32) {
+            const float x = cand[i];
+            const uint32_t k = score_key(x);
+            if (k >= lo && k <= hi) {
+              uint32_t* h = hist + ((k - lo) >> shift) * 4;
+              atomicAdd(h, 1u);
+              if (mass_mode) {
+                const unsigned long long m = mass_fixed(x, smax);
+                atomicAdd(h + 1, (uint32_t)m & kLimbMask);
+                atomicAdd(h + 2, (uint32_t)(m >> kLimbBits) & kLimbMask);
+                atomicAdd(h + 3, (uint32_t)(m >> (2 * kLimbBits)));
+              }
+            }
+          }
+          __syncwarp();
+          for (int i = lane; i < kBins; i += 32) {
+            const uint4 h = reinterpret_cast<const uint4*>(hist)[i];
+            m_cnt[i] = h.x;
+            m_mass[i] = (unsigned long long)h.y + ((unsigned long long)h.z << kLimbBits) +
+                        ((unsigned long long)h.w << (2 * kLimbBits));
+          }
+          __syncwarp();
+          pick_bin();
+          __syncwarp();
+          narrow(shift);
+          __syncwarp();
+          if (shift == 0) break;
+        }
+        if (lane == 0) {  // publish the result for the whole block
+          pick[0] = lo;
+          pick[1] = above_c;
+          pick[2] = cnt_eq;
+          pick_m[0] = above_m;
+        }
+      }
+      __syncthreads();
+      lo = pick[0];
+      above_c = pick[1];
+      cnt_eq = pick[2];
+      above_m = pick_m[0];
+    }
+  };
+  // ties at the cutoff key tau: keep the first t of the n_eq (lowest ids)
+  auto tie_take = [&](uint32_t tau, unsigned long long above_w, unsigned long long n_eq) {
+    unsigned long long t;
+    if (mass_mode) {
+      const unsigned long long w = mass_fixed(key_score(tau), smax);
+      t = w ? (target - above_w + w - 1) / w : n_eq;
+    } else {
+      t = target - above_w;
+    }
+    if (t < 1) t = 1;
+    if (t > n_eq) t = n_eq;
+    return t;
+  };
+
+  if (fast) {
+    // candidates of the cutoff bin (weights recomputed from the scores)
+    float* cand = reinterpret_cast<float*>(hist + kBins * 4);
+#pragma unroll
+    for (int k = 0; k < kPer; ++k)
+      if (k * kSelThreads + tid < N && lin_bin(v[k]) == jbin) {
+        const uint32_t idx = atomicAdd(&pick[3], 1u);
+        if (idx < kWarpCand) cand[idx] = v[k];
+      }
+    __syncthreads();
+    const uint32_t nc = pick[3];
+    if (nc <= 32) {
+      // one candidate per lane: tau is the largest key whose weight from the
+      // top, ties included, reaches the target
+      if (warp == 0) {
+        const bool has = lane < (int)nc;
+        const float cv = has ? cand[lane] : 0.f;
+        const uint32_t ck = score_key(cv);
+        const unsigned long long cm = has ? weight(cv) : 0ull;
+        unsigned long long gt_w = 0, ge_w = 0;
+        for (int o = 0; o < (int)nc; ++o) {
+          const uint32_t k2 = __shfl_sync(kFull, ck, o);
+          const unsigned long long m2 = __shfl_sync(kFull, cm, o);
+          if (k2 > ck) gt_w += m2;
+          if (k2 >= ck) ge_w += m2;
+        }
+        const bool reach = has && above_m + ge_w >= target;
+        uint32_t best = reach ? ck : 0u;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) best = max(best, __shfl_xor_sync(kFull, best, o));
+        const unsigned at = __ballot_sync(kFull, has && reach && ck == best);
+        if (lane == __ffs(at) - 1) {
+          pick[0] = best;
+          pick_m[0] = above_m + gt_w;
+        }
+      }
+      __syncthreads();
+      lo = pick[0];
+      above_m = pick_m[0];
+    } else {
+      // many candidates: the key interval of the bin, then exact radix rounds
+      uint32_t kmin = 0xffffffffu, kmax = 0u;
+#pragma unroll
+      for (int k = 0; k < kPer; ++k)
+        if (k * kSelThreads + tid < N && lin_bin(v[k]) == jbin) {
+          const uint32_t key = score_key(v[k]);
+          kmin = min(kmin, key);
+          kmax = max(kmax, key);
+        }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        kmin = min(kmin, __shfl_xor_sync(kFull, kmin, o));
+        kmax = max(kmax, __shfl_xor_sync(kFull, kmax, o));
+      }
+      if (lane == 0) {
+        red_u32[warp] = kmin;
+        red_u32[kSelWarps + warp] = kmax;
+      }
+      __syncthreads();
+      kmin = red_u32[lane];
+      kmax = red_u32[kSelWarps + lane];
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        kmin = min(kmin, __shfl_xor_sync(kFull, kmin, o));
+        kmax = max(kmax, __shfl_xor_sync(kFull, kmax, o));
+      }
+      lo = kmin;
+      hi = kmax;
+      cnt_eq = nc;
+      __syncthreads();
+      radix_resolve();
+    }
+    const uint32_t tau = lo;
+    // compaction in id order: per (slab, warp) counts of keys above and at
+    // tau, one warp-0 scan over them, then every thread writes its kept ids
+    uint32_t gtm[kPer], eqm[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const bool valid = k * kSelThreads + tid < N;
+      const uint32_t key = score_key(v[k]);
+      gtm[k] = __ballot_sync(kFull, valid && key > tau);
+      eqm[k] = __ballot_sync(kFull, valid && key == tau);
+      if (lane == 0) {
+        slab_cnt[k * kSelWarps + warp][0] = __popc(gtm[k]);
+        slab_cnt[k * kSelWarps + warp][1] = __popc(eqm[k]);
       }
     }
     __syncthreads();
-    lo = pick[0];
-    above_c = pick[1];
-    cnt_eq = pick[2];
-    above_m = pick_m[0];
+    if (warp == 0) {  // exclusive scan over the kPer * kSelWarps entries in id order
+      constexpr int kE = kPer * kSelWarps / 32;
+      uint32_t g[kE], e[kE], gs = 0, es = 0;
+#pragma unroll
+      for (int u = 0; u < kE; ++u) {
+        g[u] = slab_cnt[lane * kE + u][0];
+        e[u] = slab_cnt[lane * kE + u][1];
+        gs += g[u];
+        es += e[u];
+      }
+      uint32_t xg = gs, xe = es;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t yg = __shfl_up_sync(kFull, xg, o);
+        const uint32_t ye = __shfl_up_sync(kFull, xe, o);
+        if (lane >= o) {
+          xg += yg;
+          xe += ye;
+        }
+      }
+      uint32_t rg = xg - gs, re = xe - es;
+#pragma unroll
+      for (int u = 0; u < kE; ++u) {
+        slab_cnt[lane * kE + u][0] = rg;
+        slab_cnt[lane * kE + u][1] = re;
+        rg += g[u];
+        re += e[u];
+      }
+      if (lane == 31) {
+        pick[1] = xg;  // keys above tau
+        pick[2] = xe;  // keys at tau
+      }
+    }
+    __syncthreads();
+    const uint32_t n_gt = pick[1], n_eq = pick[2];
+    const unsigned long long t = tie_take(tau, mass_mode ? above_m : n_gt, n_eq);
+    const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const uint32_t gb = slab_cnt[k * kSelWarps + warp][0] + __popc(gtm[k] & lt);
+      const uint32_t eb = slab_cnt[k * kSelWarps + warp][1] + __popc(eqm[k] & lt);
+      const bool is_gt = (gtm[k] >> lane) & 1u, is_eq = (eqm[k] >> lane) & 1u;
+      if (is_gt || (is_eq && eb < t))
+        out[gb + (uint32_t)min((unsigned long long)eb, t)] = k * kSelThreads + tid;
+    }
+    if (tid == 0) p.lens[s] = (int32_t)(n_gt + t);
+    return;
   }
+
+  // ---- general path (N > kSelCache): the bin's key interval, exact rounds
+  {
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    for (int i = tid; i < N; i += kSelThreads) {
+      const float x = sc[i];
+      if (lin_bin(x) == jbin) {
+        const uint32_t k = score_key(x);
+        kmin = min(kmin, k);
+        kmax = max(kmax, k);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      kmin = min(kmin, __shfl_xor_sync(kFull, kmin, o));
+      kmax = max(kmax, __shfl_xor_sync(kFull, kmax, o));
+    }
+    if (lane == 0) {
+      red_u32[warp] = kmin;
+      red_u32[kSelWarps + warp] = kmax;
+    }
+    __syncthreads();
+    kmin = red_u32[lane];
+    kmax = red_u32[kSelWarps + lane];
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      kmin = min(kmin, __shfl_xor_sync(kFull, kmin, o));
+      kmax = max(kmax, __shfl_xor_sync(kFull, kmax, o));
+    }
+    lo = kmin;
+    hi = kmax;
+    __syncthreads();
+  }
+  radix_resolve();
   const uint32_t tau = lo;
-  // ties at the cutoff key: keep the first t (lowest ids)
-  unsigned long long t;
-  if (mass_mode) {
-    const unsigned long long w = mass_fixed(key_score(tau), smax);
-    t = w ? (target - above_m + w - 1) / w : cnt_eq;
-  } else {
-    t = target - above_c;
-  }
-  if (t < 1) t = 1;
-  if (t > cnt_eq) t = cnt_eq;
+  const unsigned long long t = tie_take(tau, mass_mode ? above_m : above_c, cnt_eq);
 
   // compaction in id order: thread owns ids [i0, i1)
   const int ipt = ceil_div(N, kSelThreads);
@@ -601,7 +940,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
     eq += k == tau;
   }
   // block exclusive scan of (gt, eq) packed as hi/lo 32 bits
-  unsigned long long v = ((unsigned long long)gt << 32) | eq, x = v;
+  unsigned long long pv = ((unsigned long long)gt << 32) | eq, x = pv;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const unsigned long long y = __shfl_up_sync(kFull, x, o);
@@ -619,7 +958,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
     red_u64[lane] = xx - w;  // exclusive warp offsets
   }
   __syncthreads();
-  const unsigned long long pre = red_u64[warp] + x - v;
+  const unsigned long long pre = red_u64[warp] + x - pv;
   const uint32_t gt_pre = (uint32_t)(pre >> 32), eq_pre = (uint32_t)(pre & 0xffffffffu);
   uint32_t pos = gt_pre + (uint32_t)min((unsigned long long)eq_pre, t);
   uint32_t eq_rank = eq_pre;

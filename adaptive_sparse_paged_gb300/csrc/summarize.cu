@@ -142,11 +142,15 @@ cudaError_t launch_summarize_t(const SummarizeArgs& a, cudaStream_t stream) {
     BulkParams p{kv.k_cache, kv.summaries, kv.block_table, kv.seq_lens, a.err,
                  kv.num_kv_heads, kv.max_pages, kv.num_phys_pages};
     dim3 grid(ceil_div(kv.max_pages, 8), kv.batch);
+    cudaError_t e = set_max_dynamic_smem((const void*)summarize_bulk_kernel<D, P>, 0);
+    if (e != cudaSuccess) return e;
     summarize_bulk_kernel<D, P><<<grid, 256, 0, stream>>>(p);
   } else {
     AppendParams p{kv.k_cache, kv.v_cache, kv.summaries, a.k_new, a.v_new, kv.block_table,
                    kv.seq_lens, a.err, kv.batch, kv.num_kv_heads, kv.max_pages, kv.num_phys_pages};
     const int units = kv.batch * kv.num_kv_heads;
+    cudaError_t e = set_max_dynamic_smem((const void*)summarize_append_kernel<D, P>, 0);
+    if (e != cudaSuccess) return e;
     summarize_append_kernel<D, P><<<ceil_div(units, 8), 256, 0, stream>>>(p);
   }
   return cudaGetLastError();
