@@ -328,33 +328,15 @@ __device__ __forceinline__ float key_score(uint32_t k) {
 // Softmax weight of a page relative to the top page, in 2^-37 units
 // (<= 2^37, so 8192 of them sum below 2^50 and the fast path's 19-bit limbs
 // sum below 2^32).
+// Rounded to the nearest integer with 32-bit conversions only: below 2^32
+// directly; from 2^32 on the float is already an integer, split exactly into
+// its high word and the (exact) remainder.
 __device__ __forceinline__ unsigned long long mass_fixed(float s, float smax) {
-  return __float2ull_rn(expf(s - smax) * 137438953472.0f);
-}
-
-template <typename T>
-__device__ __forceinline__ T block_reduce(T v, T* scratch, int op /*0 sum, 1 min, 2 max*/) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    const T y = __shfl_xor_sync(kFull, v, o);
-    v = op == 0 ? v + y : (op == 1 ? (y < v ? y : v) : (y > v ? y : v));
-  }
-  if (lane == 0) scratch[warp] = v;
-  __syncthreads();
-  if (warp == 0) {
-    v = scratch[lane];
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      const T y = __shfl_xor_sync(kFull, v, o);
-      v = op == 0 ? v + y : (op == 1 ? (y < v ? y : v) : (y > v ? y : v));
-    }
-    if (lane == 0) scratch[0] = v;
-  }
-  __syncthreads();
-  const T r = scratch[0];
-  __syncthreads();
-  return r;
+  const float f = expf(s - smax) * 137438953472.0f;  // 2^37
+  if (f < 4294967296.0f) return __float2uint_rn(f);
+  const uint32_t hi = __float2uint_rz(f * 2.3283064365386963e-10f);  // f / 2^32
+  const uint32_t lo = __float2uint_rz(f - (float)hi * 4294967296.0f);
+  return ((unsigned long long)hi << 32) | lo;
 }
 
 // Block min and max of one float pair in a single pass (scratch: 2 x warps).
@@ -439,27 +421,13 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
   const float smax = hi_s;
   auto weight = [&](float x) -> unsigned long long { return mass_mode ? mass_fixed(x, smax) : 1ull; };
 
-  // selection weights (fixed-point softmax mass, or 1 in budget mode) and target
+  // selection weights: fixed-point softmax mass, or 1 in budget mode. The
+  // target (gamma times the total mass) comes out of round 1's bin scan.
   unsigned long long mw[kPer];
-  unsigned long long target;
-  {
-    unsigned long long z = 0;
-    if (fast) {
+  unsigned long long target = (unsigned long long)p.budget;
+  if (fast) {
 #pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        mw[k] = k * kSelThreads + tid < N ? weight(v[k]) : 0ull;
-        z += mw[k];
-      }
-    } else if (mass_mode) {
-      for (int i = tid; i < N; i += kSelThreads) z += mass_fixed(sc[i], smax);
-    }
-    if (mass_mode) {
-      z = block_reduce<unsigned long long>(z, red_u64, 0);
-      target = (unsigned long long)ceil((double)p.gamma * (double)z);
-      if (target < 1) target = 1;
-    } else {
-      target = (unsigned long long)p.budget;
-    }
+    for (int k = 0; k < kPer; ++k) mw[k] = k * kSelThreads + tid < N ? weight(v[k]) : 0ull;
   }
 
   // state of the cutoff search: candidates are the keys in [lo, hi]; above_m
@@ -550,10 +518,16 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
       }
       red_u64[lane] = aw - w0;  // exclusive warp offsets
       red_u32[lane] = ac - c0;
+      if (lane == 31) pick_m[0] = aw;  // total weight
     }
     __syncthreads();
+    if (mass_mode) {
+      target = (unsigned long long)ceil((double)p.gamma * (double)pick_m[0]);
+      if (target < 1) target = 1;
+    }
     unsigned long long run_w = red_u64[warp] + xw - ws;
     uint32_t run_c = red_u32[warp] + xc - cs;
+    __syncthreads();  // the total has been read before pick_m is reused
     // exactly one bin has run_w < target <= run_w + w (target <= total weight)
 #pragma unroll
     for (int u = 0; u < kPb; ++u) {
@@ -566,7 +540,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
       run_w += w[u];
       run_c += c[u];
     }
-    __syncthreads();
+    __syncthreads();  // every thread has read the total; pick[] holds the bin
     jbin = (int)pick[0];
     above_m = pick_m[0];
     // counts are tracked only where the weight is not already a count
@@ -747,8 +721,16 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
   auto tie_take = [&](uint32_t tau, unsigned long long above_w, unsigned long long n_eq) {
     unsigned long long t;
     if (mass_mode) {
+      // t = ceil(rem / w): a double estimate corrected exactly (rem < 2^51)
       const unsigned long long w = mass_fixed(key_score(tau), smax);
-      t = w ? (target - above_w + w - 1) / w : n_eq;
+      const unsigned long long rem = target - above_w;
+      if (w) {
+        t = (unsigned long long)ceil((double)rem / (double)w);
+        while (t * w < rem) ++t;
+        while (t > 1 && (t - 1) * w >= rem) --t;
+      } else {
+        t = n_eq;
+      }
     } else {
       t = target - above_w;
     }
