@@ -391,6 +391,7 @@ def run_asp(args):
             "hbm_frac_of_measured": round(step_bytes / (ms / 1e3) / 1e9 / peak, 4),
             "hbm_frac_of_nominal_8tbs": round(step_bytes / (ms / 1e3) / 1e12 / 8.0, 4),
             "pages_read_frac": round(sel_pages / all_pages, 4),
+            "selected_page_heads_per_step": sel_pages,
             "bytes_per_step": step_bytes,
             "dense_gamma1": dense,
             "kernels_ms": {"select_avg": round(sel_avg_s * 1e3, 4),
