@@ -137,6 +137,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     mbar_fence_init();
     prefix[0] = 0;
   }
+  pdl_launch_dependents();
+  pdl_wait_predecessor();
   // ---- self-plan: lengths (validated) -> inclusive prefix in shared memory
   const int per = ceil_div(S, kDecThreads);
   const int a0 = min(S, tid * per), a1 = min(S, a0 + per);
@@ -499,6 +501,8 @@ struct MergeParams {
 // and folds them in with an online log-sum-exp in the log2 domain.
 __global__ void __launch_bounds__(1024) merge_kernel(const MergeParams p) {
   const int s = blockIdx.x, tid = threadIdx.x, D = p.D;
+  pdl_launch_dependents();
+  pdl_wait_predecessor();
   const int t = p.merge_table[s];
   const int cf = t >> 16, cl = t & 0xffff;
   if (cf >= cl || tid >= p.g * D) return;
@@ -586,13 +590,13 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
               a.merge_table, a.err, kv.batch, kv.num_q_heads, kv.num_kv_heads,
               kv.num_q_heads / kv.num_kv_heads, kv.max_pages, kv.num_phys_pages, a.slot_floats,
               a.sm_scale * 1.4426950408889634f};
-  decode_kernel<D, P><<<a.grid, kDecThreads, smem, stream>>>(tk, tv, p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  e = launch_pdl(decode_kernel<D, P>, dim3(a.grid), dim3(kDecThreads), smem, stream, tk, tv, p);
+  if (e != cudaSuccess) return e;
   MergeParams mp{a.partials, a.merge_table, a.out, a.lse, kv.num_q_heads, kv.num_kv_heads,
                  kv.num_q_heads / kv.num_kv_heads, D, a.slot_floats};
   if ((e = set_max_dynamic_smem((const void*)merge_kernel, 0)) != cudaSuccess) return e;
-  merge_kernel<<<S, (kv.num_q_heads / kv.num_kv_heads) * D, 0, stream>>>(mp);
-  return cudaGetLastError();
+  return launch_pdl(merge_kernel, dim3(S), dim3((kv.num_q_heads / kv.num_kv_heads) * D), 0, stream,
+                    mp);
 }
 
 }  // namespace

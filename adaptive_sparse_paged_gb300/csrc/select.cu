@@ -117,6 +117,8 @@ __global__ void __launch_bounds__(kScoreThreads, ScoreCfg<D, G>::kCtas)
     for (int i = 0; i < kSlots; ++i) mbar_init(&full[i], 1);
     mbar_fence_init();
   }
+  pdl_launch_dependents();
+  pdl_wait_predecessor();
   // prefix of the requests' page counts N_b (clamped sequence lengths)
   if (warp == 0) {
     int carry = 0;
@@ -378,6 +380,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int s = blockIdx.x;
   const int b = s / p.Hkv;
+  pdl_launch_dependents();
+  pdl_wait_predecessor();
   const int T = clamp_seq_len(p.seq_lens[b], p.max_pages, p.P, p.err);
   const int N = ceil_div(T, p.P);
   int32_t* out = p.lists + (size_t)s * p.max_pages;
@@ -967,8 +971,8 @@ cudaError_t launch_score_t(const SelectArgs& a, cudaStream_t stream) {
   cudaError_t e = set_max_dynamic_smem((const void*)score_kernel<D, G>, (int)smem);
   if (e != cudaSuccess) return e;
   // persistent: the kernel splits the pages it finds in seq_lens itself
-  score_kernel<D, G><<<C::kCtas * a.num_sms, kScoreThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(score_kernel<D, G>, dim3(C::kCtas * a.num_sms), dim3(kScoreThreads), smem,
+                    stream, p);
 }
 
 template <int D>
@@ -996,8 +1000,8 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream) {
                  kv.max_pages, a.gamma, a.budget};
   cudaError_t e = set_max_dynamic_smem((const void*)select_kernel, (int)kSelSmem);
   if (e != cudaSuccess) return e;
-  select_kernel<<<kv.batch * kv.num_kv_heads, kSelThreads, kSelSmem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(select_kernel, dim3(kv.batch * kv.num_kv_heads), dim3(kSelThreads), kSelSmem,
+                    stream, p);
 }
 
 }  // namespace asp

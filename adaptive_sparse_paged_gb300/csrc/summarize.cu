@@ -62,6 +62,8 @@ __global__ void __launch_bounds__(256) summarize_bulk_kernel(BulkParams p) {
   const int lane = threadIdx.x & 31;
   const int b = blockIdx.y;
   const int page = blockIdx.x * 8 + (threadIdx.x >> 5);
+  pdl_launch_dependents();
+  pdl_wait_predecessor();
   const int T = clamp_seq_len(p.seq_lens[b], p.max_pages, P, p.err);
   if (page >= ceil_div(T, P)) return;
   const int phys = p.bt[(size_t)b * p.max_pages + page];
@@ -110,6 +112,8 @@ __global__ void __launch_bounds__(256) summarize_append_kernel(AppendParams p) {
   constexpr int kRow = 2 * D / sizeof(V);
   const int lane = threadIdx.x & 31;
   const int unit = blockIdx.x * 8 + (threadIdx.x >> 5);  // (b, h)
+  pdl_launch_dependents();
+  pdl_wait_predecessor();
   if (unit >= p.B * p.Hkv) return;
   const int b = unit / p.Hkv, h = unit % p.Hkv;
   const int T = clamp_seq_len(p.seq_lens[b], p.max_pages, P, p.err);
@@ -144,16 +148,16 @@ cudaError_t launch_summarize_t(const SummarizeArgs& a, cudaStream_t stream) {
     dim3 grid(ceil_div(kv.max_pages, 8), kv.batch);
     cudaError_t e = set_max_dynamic_smem((const void*)summarize_bulk_kernel<D, P>, 0);
     if (e != cudaSuccess) return e;
-    summarize_bulk_kernel<D, P><<<grid, 256, 0, stream>>>(p);
+    return launch_pdl(summarize_bulk_kernel<D, P>, grid, dim3(256), 0, stream, p);
   } else {
     AppendParams p{kv.k_cache, kv.v_cache, kv.summaries, a.k_new, a.v_new, kv.block_table,
                    kv.seq_lens, a.err, kv.batch, kv.num_kv_heads, kv.max_pages, kv.num_phys_pages};
     const int units = kv.batch * kv.num_kv_heads;
     cudaError_t e = set_max_dynamic_smem((const void*)summarize_append_kernel<D, P>, 0);
     if (e != cudaSuccess) return e;
-    summarize_append_kernel<D, P><<<ceil_div(units, 8), 256, 0, stream>>>(p);
+    return launch_pdl(summarize_append_kernel<D, P>, dim3(ceil_div(units, 8)), dim3(256), 0, stream,
+                      p);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace
