@@ -51,15 +51,18 @@ constexpr int kDecWarps = 8;
 constexpr int kDecThreads = kDecWarps * 32;
 
 // A stage is a 16-token sub-tile of a page (P/16 stages per page): 8 KiB (d=128)
-// or 4 KiB (d=64). Each warp owns kSlots stages of the 128 KiB ring.
-template <int D, int P>
+// or 4 KiB (d=64). Each warp owns kSlots stages of the ring: 128 KiB per CTA,
+// or 192 KiB (Deep) when the segment prefix leaves room in shared memory.
+// While a warp computes on one stage the others stay in flight, so the extra
+// slot is what keeps each SM's share of the copy bandwidth requested.
+template <int D, int P, bool Deep>
 struct Cfg {
   static constexpr int kHalves = D / 64;
   static constexpr int kSubs = P / 16;                      // stages per page
   static constexpr int kTileBytes = 16 * 128;               // [16 rows x 64 bf16], swizzled
   static constexpr int kPartBytes = kHalves * kTileBytes;   // K (or V) of 16 tokens
   static constexpr int kStageBytes = 2 * kPartBytes;        // K then V
-  static constexpr int kSlots = D == 128 ? 2 : 4;           // stages in flight per warp
+  static constexpr int kSlots = (D == 128 ? 2 : 4) * (Deep ? 3 : 2) / 2;  // stages per warp
   static constexpr int kRingBytes = kDecWarps * kSlots * kStageBytes;
   static constexpr int kMergeFloats = kDecWarps * (2 * 8 + 8 * D);
   static constexpr int kSlotFloats = 2 * 8 + 8 * D;
@@ -113,11 +116,11 @@ __device__ __forceinline__ int cta_of(long long x, long long total, int G) {
   return (int)(((x + 1) * G - 1) / total);
 }
 
-template <int D, int P>
+template <int D, int P, bool Deep>
 __global__ void __launch_bounds__(kDecThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecParams p) {
-  using C = Cfg<D, P>;
+  using C = Cfg<D, P, Deep>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -261,6 +264,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     phB = lookup_page(32, sB, TB, lpB);
     lookup_list(64, sC, TC, lpC);
   }
+  const uint64_t pol = l2_evict_first_policy();  // K/V pages are read once
   int ib = 0;   // first warp stage of batch A
   int ni = 0;   // next warp stage to issue
   bool aborted = false;
@@ -282,9 +286,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         mbar_arrive_expect_tx(&my_full[slot], C::kStageBytes);
 #pragma unroll
         for (int hh = 0; hh < C::kHalves; ++hh) {
-          tma_load_2d(dst + hh * C::kTileBytes, &tmK, hh * 64, r_row, &my_full[slot]);
-          tma_load_2d(dst + C::kPartBytes + hh * C::kTileBytes, &tmV, hh * 64, r_row,
-                      &my_full[slot]);
+          tma_load_2d_hint(dst + hh * C::kTileBytes, &tmK, hh * 64, r_row, &my_full[slot], pol);
+          tma_load_2d_hint(dst + C::kPartBytes + hh * C::kTileBytes, &tmV, hh * 64, r_row,
+                           &my_full[slot], pol);
         }
       } else {
         mbar_arrive(&my_full[slot]);
@@ -573,14 +577,30 @@ cudaError_t make_page_map(CUtensorMap* map, const void* base, long long rows, in
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, int P>
+// Dynamic shared memory of decode_kernel: 1 KiB alignment slack, the ring,
+// the warp-merge area, per-slot metadata and mbarriers, flags, prefix[S + 1].
+template <int D, int P, bool Deep>
+size_t decode_smem_bytes(int S) {
+  using C = Cfg<D, P, Deep>;
+  return 1024 + (size_t)C::kRingBytes + C::kMergeFloats * 4 +
+         kDecWarps * C::kSlots * (sizeof(int4) + 8) + 48 * 4 + (size_t)(S + 1) * 4;
+}
+
+int max_optin_smem() {
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return 0;
+  return v;
+}
+
+template <int D, int P, bool Deep>
 cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
-  using C = Cfg<D, P>;
+  using C = Cfg<D, P, Deep>;
   const asp_paged_kv& kv = *a.kv;
   const int S = kv.batch * kv.num_kv_heads;
-  const size_t smem = 1024 + (size_t)C::kRingBytes + C::kMergeFloats * 4 +
-                      kDecWarps * C::kSlots * (sizeof(int4) + 8) + 48 * 4 + (S + 1) * 4;
-  cudaError_t e = set_max_dynamic_smem((const void*)decode_kernel<D, P>, (int)smem);
+  const size_t smem = decode_smem_bytes<D, P, Deep>(S);
+  cudaError_t e = set_max_dynamic_smem((const void*)decode_kernel<D, P, Deep>, (int)smem);
   if (e != cudaSuccess) return e;
   const long long rows = (long long)kv.num_phys_pages * kv.num_kv_heads * P;
   CUtensorMap tk, tv;
@@ -590,7 +610,7 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
               a.merge_table, a.err, kv.batch, kv.num_q_heads, kv.num_kv_heads,
               kv.num_q_heads / kv.num_kv_heads, kv.max_pages, kv.num_phys_pages, a.slot_floats,
               a.sm_scale * 1.4426950408889634f};
-  e = launch_pdl(decode_kernel<D, P>, dim3(a.grid), dim3(kDecThreads), smem, stream, tk, tv, p);
+  e = launch_pdl(decode_kernel<D, P, Deep>, dim3(a.grid), dim3(kDecThreads), smem, stream, tk, tv, p);
   if (e != cudaSuccess) return e;
   MergeParams mp{a.partials, a.merge_table, a.out, a.lse, kv.num_q_heads, kv.num_kv_heads,
                  kv.num_q_heads / kv.num_kv_heads, D, a.slot_floats};
@@ -599,16 +619,26 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
                     mp);
 }
 
+// The deeper ring when its shared memory (which grows with the segment
+// count through the prefix of list lengths) fits the device's per-block limit.
+template <int D, int P>
+cudaError_t launch_decode_dp(const DecodeArgs& a, cudaStream_t stream) {
+  const int S = a.kv->batch * a.kv->num_kv_heads;
+  if (decode_smem_bytes<D, P, true>(S) <= (size_t)max_optin_smem())
+    return launch_decode_t<D, P, true>(a, stream);
+  return launch_decode_t<D, P, false>(a, stream);
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   const int d = a.kv->head_dim, P = a.kv->page_size;
-  if (d == 128 && P == 16) return launch_decode_t<128, 16>(a, stream);
-  if (d == 128 && P == 32) return launch_decode_t<128, 32>(a, stream);
-  if (d == 128 && P == 64) return launch_decode_t<128, 64>(a, stream);
-  if (d == 64 && P == 16) return launch_decode_t<64, 16>(a, stream);
-  if (d == 64 && P == 32) return launch_decode_t<64, 32>(a, stream);
-  if (d == 64 && P == 64) return launch_decode_t<64, 64>(a, stream);
+  if (d == 128 && P == 16) return launch_decode_dp<128, 16>(a, stream);
+  if (d == 128 && P == 32) return launch_decode_dp<128, 32>(a, stream);
+  if (d == 128 && P == 64) return launch_decode_dp<128, 64>(a, stream);
+  if (d == 64 && P == 16) return launch_decode_dp<64, 16>(a, stream);
+  if (d == 64 && P == 32) return launch_decode_dp<64, 32>(a, stream);
+  if (d == 64 && P == 64) return launch_decode_dp<64, 64>(a, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -171,6 +171,7 @@ __global__ void __launch_bounds__(kScoreThreads, ScoreCfg<D, G>::kCtas)
       }
     }
   };
+  const uint64_t pol = l2_evict_first_policy();  // summaries are read once per call
   int issued = 0;
   auto issue = [&]() {  // next piece of the slice into slot issued % kSlots
     const int n = piece_pages(ic);
@@ -179,9 +180,9 @@ __global__ void __launch_bounds__(kScoreThreads, ScoreCfg<D, G>::kCtas)
     __syncwarp();
     if (lane < n) {
       const size_t page = ((size_t)ic.b * p.Hkv + ic.h) * p.max_pages + ic.lp + lane;
-      bulk_g2s(ring + slot * C::kSlotBytes + lane * kStride,
-               reinterpret_cast<const uint8_t*>(p.summ) + page * kPageBytes, kPageBytes,
-               &full[slot]);
+      bulk_g2s_hint(ring + slot * C::kSlotBytes + lane * kStride,
+                    reinterpret_cast<const uint8_t*>(p.summ) + page * kPageBytes, kPageBytes,
+                    &full[slot], pol);
     }
     advance(ic, n);
     ++issued;
