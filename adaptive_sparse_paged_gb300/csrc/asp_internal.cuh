@@ -174,6 +174,22 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ----------------------------------------------------------- even splits
+// Part i of n of [0, total): the first total % n parts hold one item more.
+// 32-bit only (total < 2^31): 64-bit division is a called routine, and at a
+// kernel's start its code fetch alone costs microseconds.
+struct EvenSplit {
+  int q, r;  // items per part, parts with one more
+  __device__ __forceinline__ EvenSplit(int total, int n) : q(total / n), r(total % n) {}
+  __device__ __forceinline__ int begin(int i) const { return i * q + min(i, r); }
+  __device__ __forceinline__ int end(int i) const { return begin(i) + q + (i < r ? 1 : 0); }
+  // part holding item x (x < total)
+  __device__ __forceinline__ int part_of(int x) const {
+    const int big = r * (q + 1);
+    return x < big ? x / (q + 1) : r + (x - big) / q;
+  }
+};
+
 // ------------------------------------------- programmatic dependent launch
 // Every kernel of the library is launched with programmatic stream
 // serialisation: the next kernel in the stream may be scheduled onto SMs as

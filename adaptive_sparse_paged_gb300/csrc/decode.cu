@@ -5,9 +5,9 @@
 //
 // Plan (every CTA, on the device): load lens[B*Hkv] into shared memory and
 // take their inclusive prefix; the concatenated lists form one sequence of
-// `total` pages, and CTA c of G takes positions [c*total/G, (c+1)*total/G).
-// Shares differ by at most one page whatever the length mix. A CTA's range
-// cuts at most two segments; each (segment, CTA) piece produces one partial
+// `total` pages, split evenly over the G CTAs (the first total % G take one
+// position more), so shares differ by at most one page whatever the length
+// mix. A CTA's range cuts at most two segments; each (segment, CTA) piece produces one partial
 // (m, l, o) in slot segment + CTA of the workspace, which is unique because
 // both indices grow along the sequence; a segment held whole by one CTA is
 // written out directly. A small second kernel merges the split segments by
@@ -111,11 +111,6 @@ __device__ __forceinline__ int seg_of(const int* prefix, int S, int pos) {
   return lo;
 }
 
-// CTA whose range [c*total/G, (c+1)*total/G) holds position x.
-__device__ __forceinline__ int cta_of(long long x, long long total, int G) {
-  return (int)(((x + 1) * G - 1) / total);
-}
-
 template <int D, int P, bool Deep>
 __global__ void __launch_bounds__(kDecThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -171,12 +166,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   for (int s = a0; s < a1; ++s) prefix[s + 1] += off;
   __syncthreads();
 
-  const long long total = prefix[S];
-  const int geff = (int)(total < G ? total : G);
+  const int total = prefix[S];  // < 2^31, checked on the host
+  const int geff = total < G ? total : G;
+  const EvenSplit split(total, geff > 0 ? geff : 1);
   long long beg = 0, end = 0;
   if (cta < geff) {
-    beg = (long long)cta * total / geff;
-    end = (long long)(cta + 1) * total / geff;
+    beg = split.begin(cta);
+    end = split.end(cta);
   }
   const float kLn2 = 0.69314718055994530942f;
 
@@ -194,7 +190,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     for (int s = tid; s < S; s += kDecThreads) {
       int t = 0;
       if (prefix[s + 1] > prefix[s]) {
-        const int cf = cta_of(prefix[s], total, geff), cl = cta_of(prefix[s + 1] - 1, total, geff);
+        const int cf = split.part_of(prefix[s]), cl = split.part_of(prefix[s + 1] - 1);
         t = (cf << 16) | cl;
       }
       p.merge_table[s] = t;

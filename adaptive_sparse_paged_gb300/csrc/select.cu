@@ -139,10 +139,9 @@ __global__ void __launch_bounds__(kScoreThreads, ScoreCfg<D, G>::kCtas)
   }
   __syncthreads();
   // this warp's slice of the Hkv * sum_b N_b pages (< 2^31, checked on the host)
-  const long long units = (long long)p.Hkv * rprefix[p.B];
-  const long long nw = (long long)gridDim.x * kScoreWarps;
-  const long long gw = (long long)blockIdx.x * kScoreWarps + warp;
-  const int wbeg = (int)(gw * units / nw), wend = (int)((gw + 1) * units / nw);
+  const EvenSplit split(p.Hkv * rprefix[p.B], gridDim.x * kScoreWarps);
+  const int gw = blockIdx.x * kScoreWarps + warp;
+  const int wbeg = split.begin(gw), wend = split.end(gw);
   if (wbeg >= wend) return;
 
   auto seg_pages = [&](int b) { return rprefix[b + 1] - rprefix[b]; };
@@ -331,15 +330,41 @@ __device__ __forceinline__ float key_score(uint32_t k) {
 // Softmax weight of a page relative to the top page, in 2^-37 units
 // (<= 2^37, so 8192 of them sum below 2^50 and the fast path's 19-bit limbs
 // sum below 2^32).
-// Rounded to the nearest integer with 32-bit conversions only: below 2^32
-// directly; from 2^32 on the float is already an integer, split exactly into
-// its high word and the (exact) remainder.
+// Rounded to the nearest integer (ties to even) by IEEE bit arithmetic on
+// the integer pipes, which have several times the throughput of the
+// conversion unit: below 2^22, adding 2^23 leaves the rounded integer in the
+// mantissa bits; from 2^23 on the float is an integer, its mantissa shifted
+// by the exponent; the band between takes one conversion instruction.
 __device__ __forceinline__ unsigned long long mass_fixed(float s, float smax) {
   const float f = expf(s - smax) * 137438953472.0f;  // 2^37
-  if (f < 4294967296.0f) return __float2uint_rn(f);
-  const uint32_t hi = __float2uint_rz(f * 2.3283064365386963e-10f);  // f / 2^32
-  const uint32_t lo = __float2uint_rz(f - (float)hi * 4294967296.0f);
-  return ((unsigned long long)hi << 32) | lo;
+  if (f < 4194304.0f) return __float_as_uint(f + 8388608.0f) & 0x7fffffu;
+  if (f >= 8388608.0f) {
+    const uint32_t u = __float_as_uint(f);
+    return (unsigned long long)((u & 0x7fffffu) | 0x800000u) << (((u >> 23) & 0xffu) - 150u);
+  }
+  return __float2uint_rn(f);
+}
+
+// ceil(gamma * z) exactly, for 0 < gamma <= 1 and z < 2^52, in integers:
+// gamma = m * 2^-k with a 24-bit m, so gamma * z = (m * z) >> k rounded up
+// (the product needs up to 76 bits: high and low 64-bit words).
+__device__ __forceinline__ unsigned long long ceil_gamma_times(float gamma, unsigned long long z) {
+  const uint32_t u = __float_as_uint(gamma);
+  const uint32_t e = (u >> 23) & 0xffu;  // gamma >= 2^-126 is normal for every gamma passed
+  const unsigned long long m = (u & 0x7fffffu) | 0x800000u;
+  const int k = 150 - (int)e;  // gamma = m * 2^-k, k >= 23 for gamma <= 1
+  const unsigned long long lo = m * z, hi = __umul64hi(m, z);
+  if (k >= 128) return (lo | hi) ? 1ull : 0ull;
+  unsigned long long q;  // (hi:lo) >> k
+  bool rem;
+  if (k >= 64) {
+    q = hi >> (k - 64);
+    rem = lo != 0 || (k > 64 && (hi & ((1ull << (k - 64)) - 1ull)) != 0);
+  } else {
+    q = (lo >> k) | (k ? hi << (64 - k) : 0ull);
+    rem = (lo & ((1ull << k) - 1ull)) != 0;
+  }
+  return q + (rem ? 1ull : 0ull);
 }
 
 // Block min and max of one float pair in a single pass (scratch: 2 x warps).
@@ -376,6 +401,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
   __shared__ float red_f[2 * kSelWarps];
   __shared__ uint32_t pick[4];
   __shared__ unsigned long long pick_m[1];
+  __shared__ unsigned long long sel_target, tie_t;  // computed by one thread
   __shared__ uint32_t slab_cnt[kPer * kSelWarps][2];  // fast compaction: (gt, eq) per (slab, warp)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -523,16 +549,19 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
       }
       red_u64[lane] = aw - w0;  // exclusive warp offsets
       red_u32[lane] = ac - c0;
-      if (lane == 31) pick_m[0] = aw;  // total weight
+      if (lane == 31) {  // gamma times the total weight, once (fp64 is slow on this part)
+        unsigned long long tg = target;
+        if (mass_mode) {
+          tg = ceil_gamma_times(p.gamma, aw);
+          if (tg < 1) tg = 1;
+        }
+        sel_target = tg;
+      }
     }
     __syncthreads();
-    if (mass_mode) {
-      target = (unsigned long long)ceil((double)p.gamma * (double)pick_m[0]);
-      if (target < 1) target = 1;
-    }
+    target = sel_target;
     unsigned long long run_w = red_u64[warp] + xw - ws;
     uint32_t run_c = red_u32[warp] + xc - cs;
-    __syncthreads();  // the total has been read before pick_m is reused
     // exactly one bin has run_w < target <= run_w + w (target <= total weight)
 #pragma unroll
     for (int u = 0; u < kPb; ++u) {
@@ -726,12 +755,13 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
   auto tie_take = [&](uint32_t tau, unsigned long long above_w, unsigned long long n_eq) {
     unsigned long long t;
     if (mass_mode) {
-      // t = ceil(rem / w): a double estimate corrected exactly (rem < 2^51)
+      // t = ceil(rem / w): a float estimate corrected exactly in integers
       const unsigned long long w = mass_fixed(key_score(tau), smax);
       const unsigned long long rem = target - above_w;
       if (w) {
-        t = (unsigned long long)ceil((double)rem / (double)w);
-        while (t * w < rem) ++t;
+        const float est = ceilf((float)rem / (float)w);
+        t = est > (float)n_eq ? n_eq : (unsigned long long)est;
+        while (t < n_eq && t * w < rem) ++t;
         while (t > 1 && (t - 1) * w >= rem) --t;
       } else {
         t = n_eq;
@@ -862,12 +892,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
       }
       if (lane == 31) {
         pick[1] = xg;  // keys above tau
-        pick[2] = xe;  // keys at tau
+        tie_t = tie_take(tau, mass_mode ? above_m : xg, xe);
       }
     }
     __syncthreads();
-    const uint32_t n_gt = pick[1], n_eq = pick[2];
-    const unsigned long long t = tie_take(tau, mass_mode ? above_m : n_gt, n_eq);
+    const uint32_t n_gt = pick[1];
+    const unsigned long long t = tie_t;
     const unsigned lt = (1u << lane) - 1u;
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
@@ -915,7 +945,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
   }
   radix_resolve();
   const uint32_t tau = lo;
-  const unsigned long long t = tie_take(tau, mass_mode ? above_m : above_c, cnt_eq);
+  if (tid == 0) tie_t = tie_take(tau, mass_mode ? above_m : above_c, cnt_eq);
+  __syncthreads();
+  const unsigned long long t = tie_t;
 
   // compaction in id order: thread owns ids [i0, i1)
   const int ipt = ceil_div(N, kSelThreads);
