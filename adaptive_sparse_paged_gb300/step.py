@@ -86,3 +86,79 @@ class DecodeStep:
 
     def replay(self):
         self.graph.replay()
+
+
+class DecodeLoop:
+    """n consecutive decode steps over L layers, captured into one CUDA graph.
+
+    Step i appends one token per request at position T0_b + i (APPEND: its K
+    and V rows, folded into its page's summary), then runs every layer's
+    coverage selection and attention with that step's queries; the page lists
+    change from step to step as the queries and the newest pages do (MOIRA
+    abstract: lists per request, layer, KV head and step). Each step has its own
+    length buffer (T0 + i + 1) and its own outputs, so the steps are unrolled
+    in the graph rather than indexed by a device counter.
+
+    The block tables must already map the pages of T0 + n tokens, and the
+    summaries must describe the first T0 tokens when the loop first runs.
+    Replaying the graph re-times the same work: the appends are idempotent,
+    but a replayed step's last-page summary then already holds the later
+    steps' tokens, so only the first run's lists are those of fresh steps.
+    """
+
+    def __init__(self, kvs, seq_lens0, q, k_new, v_new, gamma: float, budget: int = 0,
+                 sm_scale: float | None = None):
+        """kvs: PagedKV per layer; seq_lens0: int32 [B] (T0); q: fp32 [n, L, B, Hq, d];
+        k_new, v_new: bf16 [n, L, B, Hkv, d]."""
+        kv0 = kvs[0]
+        n, L = q.shape[0], len(kvs)
+        assert q.shape == (n, L, kv0.batch, kv0.num_q_heads, kv0.head_dim)
+        assert k_new.shape == (n, L, kv0.batch, kv0.num_kv_heads, kv0.head_dim)
+        assert v_new.shape == k_new.shape
+        dev = kv0.device
+        self.n, self.L = n, L
+        self.q, self.k_new, self.v_new = q, k_new, v_new
+        self.gamma, self.budget = float(gamma), int(budget)
+        self.sm_scale = sm_scale if sm_scale is not None else 1.0 / math.sqrt(kv0.head_dim)
+        self.seq_lens = [(seq_lens0 + (i + 1)).to(torch.int32).contiguous() for i in range(n)]
+        self.kvs = [[B.PagedKV(kv.k_cache, kv.v_cache, kv.summaries, kv.block_table,
+                               self.seq_lens[i], kv.num_q_heads) for kv in kvs] for i in range(n)]
+        self.lists = torch.zeros((n, L, kv0.batch, kv0.num_kv_heads, kv0.max_pages),
+                                 dtype=torch.int32, device=dev)
+        self.lens = torch.zeros((n, L, kv0.batch, kv0.num_kv_heads), dtype=torch.int32, device=dev)
+        self.out = torch.zeros((n, L, kv0.batch, kv0.num_q_heads, kv0.head_dim),
+                               dtype=torch.float32, device=dev)
+        self.lse = torch.zeros((n, L, kv0.batch, kv0.num_q_heads), dtype=torch.float32,
+                               device=dev)
+        self.ws = B.new_workspace(kv0)
+        self.graph = None
+
+    @property
+    def launches(self) -> int:
+        """Kernel launches of the whole loop: append, score, select, decode, merge."""
+        per = 2 if (self.budget > 0 or self.gamma < 1.0) else 1
+        return self.n * self.L * (1 + per + 2)
+
+    def run(self, stream=None):
+        for i in range(self.n):
+            for l in range(self.L):
+                kv = self.kvs[i][l]
+                B.asp_page_summarize(kv, B.ASP_SUMMARIZE_APPEND, self.k_new[i, l],
+                                     self.v_new[i, l], self.ws, stream)
+                B.asp_coverage_select(kv, self.q[i, l], self.gamma, self.budget,
+                                      self.lists[i, l], self.lens[i, l], self.ws, stream)
+                B.asp_sparse_decode(kv, self.q[i, l], self.lists[i, l], self.lens[i, l],
+                                    self.sm_scale, self.out[i, l], self.lse[i, l], self.ws,
+                                    stream)
+
+    def capture(self):
+        """Captures the loop into one CUDA graph. The capture itself launches
+        nothing, so the first replay is the loop's first (fresh) run."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run()
+        self.graph = g
+        return g
+
+    def replay(self):
+        self.graph.replay()

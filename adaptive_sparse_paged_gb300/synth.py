@@ -25,6 +25,10 @@ are not used, these seeded draws stand in for them:
   "frac" draws a fraction log-uniform in [0.5%, 50%] of N_b (at least 1).
 * Sequence lengths: fixed, or log-normal (median 16384, sigma 1) clipped to
   [4096, 131072] and not rounded to the page size (partial last pages).
+* Multi-step decoding: step i's queries are the layer's queries plus
+  sigma * N(0, 1) noise (sigma 0.25), so consecutive steps stay correlated
+  while their page lists vary; each step appends one token per request whose
+  key and value are N(0, 1) in bf16.
 """
 
 from __future__ import annotations
@@ -159,3 +163,24 @@ def make_layer(w: Workload, sh: Shared, seed: int, layer: int, device) -> Layer:
             k[phys, h] = blk.to(torch.bfloat16)
             hot[(b, h)] = sorted(int(x) for x in pages)
     return Layer(k, v, q, hot)
+
+
+@dataclass
+class Steps:
+    q: torch.Tensor       # fp32 [n, L, B, Hq, d]
+    k_new: torch.Tensor   # bf16 [n, L, B, Hkv, d]
+    v_new: torch.Tensor
+
+
+def make_steps(w: Workload, layer_q, n: int, seed: int, device, sigma: float = 0.25) -> Steps:
+    """Inputs of n consecutive decode steps: per-step queries (the layers'
+    queries plus sigma * N(0, 1)) and the tokens each step appends."""
+    L = len(layer_q)
+    base = torch.stack(list(layer_q))  # [L, B, Hq, d]
+    g = _gen(seed, 20, device=device)
+    q = base.unsqueeze(0) + sigma * torch.randn((n,) + tuple(base.shape), generator=g,
+                                                device=device, dtype=torch.float32)
+    shape = (n, L, w.batch, w.num_kv_heads, w.head_dim)
+    k_new = torch.randn(shape, generator=g, device=device, dtype=torch.bfloat16)
+    v_new = torch.randn(shape, generator=g, device=device, dtype=torch.bfloat16)
+    return Steps(q.contiguous(), k_new, v_new)

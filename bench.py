@@ -49,6 +49,9 @@ def parse_args(argv=None):
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
+    ap.add_argument("--no-multistep", action="store_true")
+    ap.add_argument("--multistep-steps", type=int, default=8,
+                    help="decode steps unrolled in the multi-step graph")
     ap.add_argument("--oracle-segments", type=int, default=0,
                     help="segments per oracle sample (default: host cores, at least 8)")
     return ap.parse_args(argv)
@@ -186,12 +189,16 @@ def start_oracle_pool():
 
 
 def oracle_sample_tasks(w, sh, layer, nseg, gamma, budget, seed):
-    """Seeded sample of (request, KV head) segments of one layer, as oracle inputs."""
+    """Seeded sample of (request, KV head) segments of one layer, as oracle inputs
+    (every segment of the layer when nseg covers them all)."""
     import numpy as np
     import torch
     rng = np.random.default_rng(seed)
     segs = [(b, h) for b in range(w.batch) for h in range(w.num_kv_heads)]
-    pick = [segs[i] for i in rng.choice(len(segs), min(nseg, len(segs)), replace=False)]
+    if nseg >= len(segs):
+        pick = segs
+    else:
+        pick = [segs[i] for i in rng.choice(len(segs), nseg, replace=False)]
     g = w.num_q_heads // w.num_kv_heads
     q = layer.q.double().cpu().numpy()
     tasks = []
@@ -223,7 +230,7 @@ def run_asp(args):
 
     from adaptive_sparse_paged_gb300 import binding as B
     from adaptive_sparse_paged_gb300 import synth
-    from adaptive_sparse_paged_gb300.step import DecodeStep
+    from adaptive_sparse_paged_gb300.step import DecodeLoop, DecodeStep
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -347,18 +354,55 @@ def run_asp(args):
            "h2d_bytes_per_step": int(q_host.numel() * 4),
            "d2h_bytes_per_step": int(out_host.numel() * 4 + lse_host.numel() * 4)}
 
+    # Several decode steps in one graph: step i appends one token per request
+    # (the last n tokens of the context are replayed as n appends) and runs
+    # every layer with its own queries, so the page lists vary from step to step.
+    multi = None
+    if not args.no_multistep and args.multistep_steps > 0:
+        n_ms = args.multistep_steps
+        full_lens = sh.seq_lens.clone()
+        t0 = (full_lens - n_ms).clamp(min=0)
+        sh.seq_lens.copy_(t0)
+        for kv in kvs:  # summaries of the first T0 tokens
+            B.asp_page_summarize(kv, B.ASP_SUMMARIZE_BULK, None, None, ws0)
+        steps_in = synth.make_steps(w, [lay.q for lay in layers], n_ms, seed, dev)
+        loop = DecodeLoop(kvs, t0.clone(), steps_in.q, steps_in.k_new, steps_in.v_new,
+                          gamma=args.gamma)
+        loop.capture()
+        loop.replay()  # the first run: fresh steps
+        torch.cuda.synchronize()
+        assert B.asp_get_device_error(loop.ws) == 0
+        lens_ms = loop.lens.cpu().numpy().astype(np.int64)  # [n, L, B, Hkv]
+        Km = max(3, args.steps // 20)
+        t_ms = max_over_ranks(timed_graph(loop, Km, 3), dist, dev)
+        sh.seq_lens.copy_(full_lens)  # the appended tokens are now the context's last ones
+        torch.cuda.synchronize()
+        tpot = t_ms / (Km * n_ms)
+        frac = [round(float(lens_ms[i].sum()) / all_pages, 4) for i in range(n_ms)]
+        multi = {"steps_in_graph": n_ms, "append": True, "tpot_ms": round(1e3 * tpot, 4),
+                 "steps_per_s": round(world / tpot, 3), "replays": Km,
+                 "pages_read_frac_by_step": frac,
+                 "launches_per_graph": loop.launches,
+                 "query_change": "per step: layer queries + 0.25 * N(0, 1)"}
+        del loop, steps_in
+
     cpu = None
     if pool is not None:
-        nseg = args.oracle_segments or max(8, cores)
-        tasks = oracle_sample_tasks(w, sh, layers[0], nseg, args.gamma, 0, args.seed)
+        # two whole layers (every segment of layers 0 and 1), scaled to all L layers
+        nl = min(2, w.layers)
+        seg_layer = w.batch * w.num_kv_heads
+        tasks = []
+        for l in range(nl):
+            tasks += oracle_sample_tasks(w, sh, layers[l], seg_layer, args.gamma, 0, args.seed)
         time_oracle(pool, tasks[:min(len(tasks), cores)])  # warm the workers
         t_cpu = time_oracle(pool, tasks)
-        segs_per_step = w.batch * w.num_kv_heads * w.layers
+        segs_per_step = seg_layer * w.layers
         step_s = t_cpu * segs_per_step / len(tasks)
         cpu = {"value": 1.0 / step_s, "unit": "steps/s", "cores": cores, "kind": "oracle",
-               "sample": f"{len(tasks)} of {segs_per_step} (request, KV head, layer) segments "
-                         f"of layer 0, full context each, fp64 numpy, {cores} spawn workers "
-                         f"x 1 thread; {t_cpu:.1f} s scaled to a full step"}
+               "sample": f"layers 0-{nl - 1} in full ({len(tasks)} of {segs_per_step} "
+                         f"(request, KV head, layer) segments, full context each), fp64 numpy, "
+                         f"{cores} spawn workers x 1 thread, inputs pickled to the workers; "
+                         f"{t_cpu:.1f} s, extrapolated x{w.layers / nl:g} to a full step"}
         pool.close()
 
     if rank == 0:
@@ -394,6 +438,7 @@ def run_asp(args):
             "selected_page_heads_per_step": sel_pages,
             "bytes_per_step": step_bytes,
             "dense_gamma1": dense,
+            "multi_step": multi,
             "kernels_ms": {"select_avg": round(sel_avg_s * 1e3, 4),
                            "decode_avg": round(dec_avg_s * 1e3, 4)},
             "roofline": {
