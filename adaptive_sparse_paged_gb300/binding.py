@@ -32,6 +32,7 @@ EXPORTED = (
     "asp_workspace_init",
     "asp_page_summarize",
     "asp_coverage_select",
+    "asp_page_scores",
     "asp_sparse_decode",
     "asp_get_device_error",
     "asp_coverage_select_noalloc",
@@ -85,6 +86,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "asp_workspace_init": ([vp, sz, vp], i32),
             "asp_page_summarize": ([kvp, i32, vp, vp, vp, sz, vp], i32),
             "asp_coverage_select": ([kvp, vp, ctypes.c_float, i32, vp, vp, vp, sz, vp], i32),
+            "asp_page_scores": ([kvp, vp, vp, vp, sz, vp], i32),
             "asp_sparse_decode": ([kvp, vp, vp, vp, ctypes.c_float, vp, vp, vp, sz, vp], i32),
             "asp_get_device_error": ([vp, u32p, vp], i32),
             "asp_coverage_select_noalloc": ([kvp, vp, ctypes.c_float, i32, vp, vp, vp, vp], i32),
@@ -222,6 +224,20 @@ def asp_coverage_select(kv: PagedKV, q: torch.Tensor, gamma: float, budget: int,
             kv.ref, q.data_ptr(), ctypes.c_float(gamma), int(budget), lists.data_ptr(),
             lens.data_ptr(), ws.data_ptr(), ws.numel(), _stream_ptr(kv.device, stream)),
             "asp_coverage_select")
+
+
+def asp_page_scores(kv: PagedKV, q: torch.Tensor, scores: torch.Tensor, ws: torch.Tensor,
+                    stream=None) -> None:
+    """Per-page scores [B, Hkv, max_pages] fp32 (entries past N_b untouched)."""
+    _need(q, "q", torch.float32, kv.device, (kv.batch, kv.num_q_heads, kv.head_dim))
+    _need(scores, "scores", torch.float32, kv.device,
+          (kv.batch, kv.num_kv_heads, kv.max_pages))
+    _need(ws, "ws", torch.uint8, kv.device)
+    with torch.cuda.device(kv.device):
+        _check(load_library().asp_page_scores(kv.ref, q.data_ptr(), scores.data_ptr(),
+                                              ws.data_ptr(), ws.numel(),
+                                              _stream_ptr(kv.device, stream)),
+               "asp_page_scores")
 
 
 def asp_sparse_decode(kv: PagedKV, q: torch.Tensor, lists: torch.Tensor, lens: torch.Tensor,

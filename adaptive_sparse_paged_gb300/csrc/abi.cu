@@ -165,6 +165,20 @@ asp_status asp_coverage_select(const asp_paged_kv* kv, const float* q, float gam
   return from_cuda(launch_select(a, static_cast<cudaStream_t>(stream)));
 }
 
+asp_status asp_page_scores(const asp_paged_kv* kv, const float* q, float* scores, void* ws,
+                           size_t ws_bytes, asp_stream stream) {
+  asp_status st = check_kv(kv);
+  if (st != ASP_OK) return st;
+  if (!q || !scores) return ASP_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(q) & 15u) || (reinterpret_cast<uintptr_t>(scores) & 3u))
+    return ASP_EINVAL;
+  WsLayout lay;
+  if ((st = check_ws(kv, ws, ws_bytes, &lay)) != ASP_OK) return st;
+  SelectArgs a{kv, q, 0.5f, 0, nullptr, nullptr, scores, static_cast<uint32_t*>(ws),
+               current_device_sm_count()};
+  return from_cuda(launch_scores(a, static_cast<cudaStream_t>(stream)));
+}
+
 asp_status asp_sparse_decode(const asp_paged_kv* kv, const float* q, const int32_t* lists,
                              const int32_t* lens, float sm_scale, float* out, float* lse,
                              void* ws, size_t ws_bytes, asp_stream stream) {

@@ -280,6 +280,8 @@ struct SelectArgs {
   int num_sms;
 };
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream);
+// The score kernel alone (a.scores: [B, Hkv, max_pages]; lists/lens unused).
+cudaError_t launch_scores(const SelectArgs& a, cudaStream_t stream);
 
 struct DecodeArgs {
   const asp_paged_kv* kv;

@@ -1021,12 +1021,15 @@ cudaError_t launch_score_d(const SelectArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
+cudaError_t launch_scores(const SelectArgs& a, cudaStream_t stream) {
+  return a.kv->head_dim == 128 ? launch_score_d<128>(a, stream) : launch_score_d<64>(a, stream);
+}
+
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream) {
   const asp_paged_kv& kv = *a.kv;
   const bool all = a.budget <= 0 && a.gamma >= 1.0f;
   if (!all) {  // gamma >= 1 keeps every page: no scores needed
-    cudaError_t e = kv.head_dim == 128 ? launch_score_d<128>(a, stream)
-                                       : launch_score_d<64>(a, stream);
+    cudaError_t e = launch_scores(a, stream);
     if (e != cudaSuccess) return e;
   }
   SelectParams p{a.scores, kv.seq_lens, a.lists, a.lens, a.err, kv.num_kv_heads, kv.page_size,

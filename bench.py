@@ -50,6 +50,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-multistep", action="store_true")
+    ap.add_argument("--no-diagnostics", action="store_true")
     ap.add_argument("--multistep-steps", type=int, default=8,
                     help="decode steps unrolled in the multi-step graph")
     ap.add_argument("--oracle-segments", type=int, default=0,
@@ -354,6 +355,12 @@ def run_asp(args):
            "h2d_bytes_per_step": int(q_host.numel() * 4),
            "d2h_bytes_per_step": int(out_host.numel() * 4 + lse_host.numel() * 4)}
 
+    # required page fractions per gamma, and a fixed budget of equal bytes
+    diag = None
+    if not args.no_diagnostics:
+        from adaptive_sparse_paged_gb300 import diagnostics as Dg
+        diag = Dg.budget_diagnostics(kvs, q_all, ref_gamma=args.gamma)
+
     # Several decode steps in one graph: step i appends one token per request
     # (the last n tokens of the context are replayed as n appends) and runs
     # every layer with its own queries, so the page lists vary from step to step.
@@ -439,6 +446,7 @@ def run_asp(args):
             "bytes_per_step": step_bytes,
             "dense_gamma1": dense,
             "multi_step": multi,
+            "budget_diagnostics": diag,
             "kernels_ms": {"select_avg": round(sel_avg_s * 1e3, 4),
                            "decode_avg": round(dec_avg_s * 1e3, 4)},
             "roofline": {

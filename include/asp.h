@@ -177,6 +177,21 @@ asp_status asp_coverage_select(const asp_paged_kv* kv, const float* q, float gam
                                void* ws, size_t ws_bytes, asp_stream stream);
 
 /*
+ * Page scores alone: the estimate that asp_coverage_select ranks (MOIRA
+ * abstract: "estimated attention mass" per page; the Quest bound as named in
+ * the HiSparse abstract), for diagnostics such as the captured mass of a
+ * fixed page budget. For each segment (b, kv head h) and page p < N_b:
+ *   scores[b, h, p] = (1/sqrt(d)) * max over the group of
+ *                     sum_i max(q_i * min_pi, q_i * max_pi)        (fp32)
+ * q      : fp32 [B, Hq, d], 16-byte aligned.
+ * scores : fp32 [B, Hkv, max_pages] out; entries p >= N_b are untouched.
+ * Runs the same kernel as asp_coverage_select's first pass; the workspace
+ * supplies only the device error word.
+ */
+asp_status asp_page_scores(const asp_paged_kv* kv, const float* q, float* scores, void* ws,
+                           size_t ws_bytes, asp_stream stream);
+
+/*
  * Self-planning sparse attention (MOIRA abstract: each thread block derives
  * its own share of the work from the list lengths, so the step stays inside
  * the CUDA graph).

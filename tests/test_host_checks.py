@@ -43,6 +43,7 @@ def test_bad_shapes_rejected(lib, over, want):
     assert lib.asp_sparse_decode(ctypes.byref(s), FAKE, FAKE, FAKE, 0.1, FAKE, FAKE, FAKE,
                                  1 << 20, None) == want
     assert lib.asp_page_summarize(ctypes.byref(s), 0, None, None, FAKE, 1 << 20, None) == want
+    assert lib.asp_page_scores(ctypes.byref(s), FAKE, FAKE, FAKE, 1 << 20, None) == want
 
 
 @pytest.mark.parametrize("gamma,budget", [(0.0, 0), (-0.5, 0), (1.5, 0), (float("nan"), 0),
@@ -63,6 +64,9 @@ def test_null_outputs_and_modes(lib):
     assert lib.asp_page_summarize(ctypes.byref(s), 7, None, None, FAKE, 1, None) == B.ASP_EINVAL
     assert lib.asp_page_summarize(ctypes.byref(s), 1, None, None, FAKE, 1, None) == B.ASP_EINVAL
     assert lib.asp_page_summarize(ctypes.byref(s), 0, FAKE, FAKE, FAKE, 1, None) == B.ASP_EINVAL
+    assert lib.asp_page_scores(ctypes.byref(s), None, FAKE, FAKE, 1, None) == B.ASP_EINVAL
+    assert lib.asp_page_scores(ctypes.byref(s), FAKE, None, FAKE, 1, None) == B.ASP_EINVAL
+    assert lib.asp_page_scores(ctypes.byref(s), FAKE + 4, FAKE, FAKE, 1, None) == B.ASP_EINVAL
 
 
 def test_workspace_pointer_checks(lib):
