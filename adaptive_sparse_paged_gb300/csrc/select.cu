@@ -213,7 +213,8 @@ __global__ void __launch_bounds__(kScoreThreads, ScoreCfg<D, G>::kCtas)
         }
       }
   };
-  int qseg = -1, k = 0;
+  int qseg = cc.b * p.Hkv + cc.h, k = 0;
+  load_q(cc.b, cc.h);  // the first piece's queries load while its copies fly
   bool aborted = false;
   const uint32_t lane_row = (uint32_t)((lane & 7) * kStride + (lane >> 3) * 16);
 #pragma unroll 1
@@ -336,7 +337,7 @@ __device__ __forceinline__ float key_score(uint32_t k) {
 // mantissa bits; from 2^23 on the float is an integer, its mantissa shifted
 // by the exponent; the band between takes one conversion instruction.
 __device__ __forceinline__ unsigned long long mass_fixed(float s, float smax) {
-  const float f = expf(s - smax) * 137438953472.0f;  // 2^37
+  const float f = exp2f((s - smax) * 1.4426950408889634f) * 137438953472.0f;  // 2^37
   if (f < 4194304.0f) return __float_as_uint(f + 8388608.0f) & 0x7fffffu;
   if (f >= 8388608.0f) {
     const uint32_t u = __float_as_uint(f);
@@ -522,10 +523,13 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const unsigned long long yw = __shfl_up_sync(kFull, xw, o);
-      const uint32_t yc = __shfl_up_sync(kFull, xc, o);
-      if (lane >= o) {
-        xw += yw;
-        xc += yc;
+      if (lane >= o) xw += yw;
+    }
+    if (!fast) {  // counts per bin exist only on the general path
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t yc = __shfl_up_sync(kFull, xc, o);
+        if (lane >= o) xc += yc;
       }
     }
     if (lane == 31) {
