@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
   auto weight = [&](float x) -> unsigned long long { return mass_mode ? mass_fixed(x, smax) : 1ull; };
 
   // selection weights: fixed-point softmax mass, or 1 in budget mode. The
-  // target (gamma times the total mass) comes out of round 1's bin scan.
+  // target (gamma times the total mass) comes out of the first pass's bin scan.
   unsigned long long mw[kPer];
   unsigned long long target = (unsigned long long)p.budget;
   if (fast) {
@@ -470,7 +470,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
   uint32_t* my_hist = hist + warp * kBins * 4;
   constexpr uint32_t kLimbMask = (1u << kLimbBits) - 1u;
 
-  // Round 1: one histogram of bins linear in the distance from the top score,
+  // First pass: one histogram of bins linear in the distance from the top score,
   // smax - s, over at most 28 units in mass mode (a page further down has
   // zero fixed-point mass). The bin index never increases with the score, so
   // the bin where the running weight from the top reaches the target holds
