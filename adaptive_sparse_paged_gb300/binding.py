@@ -32,6 +32,7 @@ EXPORTED = (
     "asp_workspace_init",
     "asp_page_summarize",
     "asp_coverage_select",
+    "asp_coverage_select_append",
     "asp_page_scores",
     "asp_sparse_decode",
     "asp_get_device_error",
@@ -87,6 +88,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "asp_page_summarize": ([kvp, i32, vp, vp, vp, sz, vp], i32),
             "asp_coverage_select": ([kvp, vp, ctypes.c_float, i32, vp, vp, vp, sz, vp], i32),
             "asp_page_scores": ([kvp, vp, vp, vp, sz, vp], i32),
+            "asp_coverage_select_append": ([kvp, vp, vp, vp, ctypes.c_float, i32, vp, vp, vp,
+                                            sz, vp], i32),
             "asp_sparse_decode": ([kvp, vp, vp, vp, ctypes.c_float, vp, vp, vp, sz, vp], i32),
             "asp_get_device_error": ([vp, u32p, vp], i32),
             "asp_coverage_select_noalloc": ([kvp, vp, ctypes.c_float, i32, vp, vp, vp, vp], i32),
@@ -224,6 +227,24 @@ def asp_coverage_select(kv: PagedKV, q: torch.Tensor, gamma: float, budget: int,
             kv.ref, q.data_ptr(), ctypes.c_float(gamma), int(budget), lists.data_ptr(),
             lens.data_ptr(), ws.data_ptr(), ws.numel(), _stream_ptr(kv.device, stream)),
             "asp_coverage_select")
+
+
+def asp_coverage_select_append(kv: PagedKV, k_new: torch.Tensor, v_new: torch.Tensor,
+                               q: torch.Tensor, gamma: float, budget: int, lists: torch.Tensor,
+                               lens: torch.Tensor, ws: torch.Tensor, stream=None) -> None:
+    """APPEND (k_new, v_new: bf16 [B, Hkv, d]) and coverage selection in one pass."""
+    shp = (kv.batch, kv.num_kv_heads, kv.head_dim)
+    _need(k_new, "k_new", torch.bfloat16, kv.device, shp)
+    _need(v_new, "v_new", torch.bfloat16, kv.device, shp)
+    _need(q, "q", torch.float32, kv.device, (kv.batch, kv.num_q_heads, kv.head_dim))
+    _need(lists, "lists", torch.int32, kv.device, (kv.batch, kv.num_kv_heads, kv.max_pages))
+    _need(lens, "lens", torch.int32, kv.device, (kv.batch, kv.num_kv_heads))
+    _need(ws, "ws", torch.uint8, kv.device)
+    with torch.cuda.device(kv.device):
+        _check(load_library().asp_coverage_select_append(
+            kv.ref, k_new.data_ptr(), v_new.data_ptr(), q.data_ptr(), ctypes.c_float(gamma),
+            int(budget), lists.data_ptr(), lens.data_ptr(), ws.data_ptr(), ws.numel(),
+            _stream_ptr(kv.device, stream)), "asp_coverage_select_append")
 
 
 def asp_page_scores(kv: PagedKV, q: torch.Tensor, scores: torch.Tensor, ws: torch.Tensor,

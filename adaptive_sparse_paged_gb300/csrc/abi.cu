@@ -165,6 +165,26 @@ asp_status asp_coverage_select(const asp_paged_kv* kv, const float* q, float gam
   return from_cuda(launch_select(a, static_cast<cudaStream_t>(stream)));
 }
 
+asp_status asp_coverage_select_append(const asp_paged_kv* kv, const uint16_t* k_new,
+                                      const uint16_t* v_new, const float* q, float gamma,
+                                      int32_t budget, int32_t* lists, int32_t* lens, void* ws,
+                                      size_t ws_bytes, asp_stream stream) {
+  asp_status st = check_kv(kv);
+  if (st != ASP_OK) return st;
+  if (!q || !lists || !lens || !k_new || !v_new) return ASP_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_new) |
+       reinterpret_cast<uintptr_t>(v_new)) & 15u)
+    return ASP_EINVAL;
+  if (budget < 0) return ASP_EINVAL;
+  if (budget == 0 && !(gamma > 0.0f && gamma <= 1.0f)) return ASP_EINVAL;
+  WsLayout lay;
+  if ((st = check_ws(kv, ws, ws_bytes, &lay)) != ASP_OK) return st;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  SelectArgs a{kv, q, gamma, budget, lists, lens, reinterpret_cast<float*>(w + lay.scores_off),
+               reinterpret_cast<uint32_t*>(w), current_device_sm_count(), k_new, v_new};
+  return from_cuda(launch_select(a, static_cast<cudaStream_t>(stream)));
+}
+
 asp_status asp_page_scores(const asp_paged_kv* kv, const float* q, float* scores, void* ws,
                            size_t ws_bytes, asp_stream stream) {
   asp_status st = check_kv(kv);

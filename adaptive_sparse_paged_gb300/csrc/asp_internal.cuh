@@ -222,6 +222,28 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// ------------------------------------------------------ bf16 channel min/max
+// Exact: the min or max of two bf16 values is one of them.
+__device__ __forceinline__ uint32_t bmin2(uint32_t a, uint32_t b) {
+  __nv_bfloat162 r = __hmin2(*reinterpret_cast<__nv_bfloat162*>(&a),
+                             *reinterpret_cast<__nv_bfloat162*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+  __nv_bfloat162 r = __hmax2(*reinterpret_cast<__nv_bfloat162*>(&a),
+                             *reinterpret_cast<__nv_bfloat162*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint2 vmin(uint2 a, uint2 b) {
+  return make_uint2(bmin2(a.x, b.x), bmin2(a.y, b.y));
+}
+__device__ __forceinline__ uint2 vmax(uint2 a, uint2 b) {
+  return make_uint2(bmax2(a.x, b.x), bmax2(a.y, b.y));
+}
+__device__ __forceinline__ uint32_t vmin(uint32_t a, uint32_t b) { return bmin2(a, b); }
+__device__ __forceinline__ uint32_t vmax(uint32_t a, uint32_t b) { return bmax2(a, b); }
+
+
 // ------------------------------------------------------ warp-level mma (bf16)
 // ldmatrix of four 8x8 b16 matrices; lane i supplies the row address of
 // matrix i / 8, row i % 8.
@@ -243,6 +265,12 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Orders this thread's generic-proxy global writes before its later
+// async-proxy (bulk copy) reads of the same memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // Orders this thread's generic-proxy shared-memory writes before later
@@ -278,6 +306,9 @@ struct SelectArgs {
   float* scores;
   uint32_t* err;
   int num_sms;
+  // optional fused append (asp_coverage_select_append): bf16 [B, Hkv, d]
+  const uint16_t* k_new = nullptr;
+  const uint16_t* v_new = nullptr;
 };
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream);
 // The score kernel alone (a.scores: [B, Hkv, max_pages]; lists/lens unused).

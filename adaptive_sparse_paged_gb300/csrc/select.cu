@@ -31,6 +31,8 @@
 //                overflow), which keeps hot bins from serialising the CTA.
 #include "asp_internal.cuh"
 
+#include <type_traits>
+
 namespace asp {
 namespace {
 
@@ -41,13 +43,20 @@ constexpr int kScoreWarps = 8;
 constexpr int kScoreThreads = kScoreWarps * 32;
 
 struct ScoreParams {
-  const uint16_t* summ;
+  uint16_t* summ;  // written only by the fused append
   const float* q;
   const int32_t* seq_lens;
   float* scores;
   uint32_t* err;
   int B, Hq, Hkv, P, max_pages;
   float inv_sqrt_d;
+  // fused append (null k_new: none): new token rows bf16 [B, Hkv, d]
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  uint16_t* k_cache;
+  uint16_t* v_cache;
+  const int32_t* bt;
+  int num_phys;
 };
 
 // Three bf16 terms whose sum is x to fp32 precision: s0 = rn(x),
@@ -112,6 +121,7 @@ __global__ void __launch_bounds__(kScoreThreads, ScoreCfg<D, G>::kCtas)
   uint64_t* full = reinterpret_cast<uint64_t*>(score_smem + kRingBytes) + warp * kSlots;
   int* rprefix = reinterpret_cast<int*>(score_smem + kRingBytes +
                                         kScoreWarps * kSlots * sizeof(uint64_t));  // [B + 1]
+  int* tlen = rprefix + p.B + 1;  // [B] clamped sequence lengths (for the fused append)
 
   if (lane == 0) {
     for (int i = 0; i < kSlots; ++i) mbar_init(&full[i], 1);
@@ -126,7 +136,11 @@ __global__ void __launch_bounds__(kScoreThreads, ScoreCfg<D, G>::kCtas)
     for (int b0 = 0; b0 < p.B; b0 += 32) {
       const int b = b0 + lane;
       int n = 0;
-      if (b < p.B) n = ceil_div(clamp_seq_len(p.seq_lens[b], p.max_pages, p.P, p.err), p.P);
+      if (b < p.B) {
+        const int T = clamp_seq_len(p.seq_lens[b], p.max_pages, p.P, p.err);
+        tlen[b] = T;
+        n = ceil_div(T, p.P);
+      }
       int x = n;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -172,11 +186,42 @@ __global__ void __launch_bounds__(kScoreThreads, ScoreCfg<D, G>::kCtas)
   };
   const uint64_t pol = l2_evict_first_policy();  // summaries are read once per call
   int issued = 0;
+  // Fused append (asp_coverage_select_append): before the piece that holds
+  // a segment's last page is copied, its warp writes the new token's K and V
+  // rows and folds the key into that page's summary (a fresh page, slot 0,
+  // takes the key as both bounds), exactly as the APPEND summarize does.
+  using LV = typename std::conditional<D == 128, uint2, uint32_t>::type;  // d / 32 channels
+  constexpr int kLRow = 2 * D / (int)sizeof(LV);                          // lane units per row
+  auto append_token = [&](int b, int h, int lp_last) {
+    const int T = tlen[b], slot = (T - 1) % p.P;
+    const int phys = __ldg(p.bt + (size_t)b * p.max_pages + lp_last);
+    if (phys < 0 || phys >= p.num_phys) {
+      if (lane == 0) report(p.err, ASP_DEVERR_PAGE_RANGE);
+      return;
+    }
+    const size_t unit = (size_t)b * p.Hkv + h;
+    const size_t row = ((size_t)phys * p.Hkv + h) * p.P + slot;
+    const LV kn = reinterpret_cast<const LV*>(p.k_new + unit * D)[lane];
+    const LV vn = reinterpret_cast<const LV*>(p.v_new + unit * D)[lane];
+    reinterpret_cast<LV*>(p.k_cache + row * D)[lane] = kn;
+    reinterpret_cast<LV*>(p.v_cache + row * D)[lane] = vn;
+    LV* sm = reinterpret_cast<LV*>(p.summ + (unit * p.max_pages + lp_last) * 2 * D) + lane;
+    if (slot == 0) {
+      sm[0] = kn;
+      sm[kLRow] = kn;
+    } else {
+      sm[0] = vmin(sm[0], kn);
+      sm[kLRow] = vmax(sm[kLRow], kn);
+    }
+  };
   auto issue = [&]() {  // next piece of the slice into slot issued % kSlots
     const int n = piece_pages(ic);
     const int slot = issued % kSlots;
+    const bool app = p.k_new != nullptr && ic.lp + n == seg_pages(ic.b);  // warp-uniform
+    if (app) append_token(ic.b, ic.h, ic.lp + n - 1);
     if (lane == 0) mbar_arrive_expect_tx(&full[slot], n * kPageBytes);
     __syncwarp();
+    if (app) fence_proxy_async_global();  // the fold, before this warp's copy reads the page
     if (lane < n) {
       const size_t page = ((size_t)ic.b * p.Hkv + ic.h) * p.max_pages + ic.lp + lane;
       bulk_g2s_hint(ring + slot * C::kSlotBytes + lane * kStride,
@@ -1001,10 +1046,11 @@ template <int D, int G>
 cudaError_t launch_score_t(const SelectArgs& a, cudaStream_t stream) {
   const asp_paged_kv& kv = *a.kv;
   ScoreParams p{kv.summaries, a.q, kv.seq_lens, a.scores, a.err, kv.batch, kv.num_q_heads,
-                kv.num_kv_heads, kv.page_size, kv.max_pages, 1.0f / sqrtf((float)D)};
+                kv.num_kv_heads, kv.page_size, kv.max_pages, 1.0f / sqrtf((float)D),
+                a.k_new, a.v_new, kv.k_cache, kv.v_cache, kv.block_table, kv.num_phys_pages};
   using C = ScoreCfg<D, G>;
   const size_t smem = (size_t)kScoreWarps * C::kSlots * (C::kSlotBytes + sizeof(uint64_t)) +
-                      (kv.batch + 1) * sizeof(int);
+                      (2 * kv.batch + 1) * sizeof(int);
   cudaError_t e = set_max_dynamic_smem((const void*)score_kernel<D, G>, (int)smem);
   if (e != cudaSuccess) return e;
   // persistent: the kernel splits the pages it finds in seq_lens itself
@@ -1032,7 +1078,7 @@ cudaError_t launch_scores(const SelectArgs& a, cudaStream_t stream) {
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream) {
   const asp_paged_kv& kv = *a.kv;
   const bool all = a.budget <= 0 && a.gamma >= 1.0f;
-  if (!all) {  // gamma >= 1 keeps every page: no scores needed
+  if (!all || a.k_new) {  // gamma >= 1 keeps every page: no scores needed (but the append)
     cudaError_t e = launch_scores(a, stream);
     if (e != cudaSuccess) return e;
   }

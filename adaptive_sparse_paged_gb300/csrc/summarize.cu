@@ -26,25 +26,6 @@ struct LaneVec<64> {
   using T = uint32_t;  // 2 channels
 };
 
-__device__ __forceinline__ uint32_t bmin2(uint32_t a, uint32_t b) {
-  __nv_bfloat162 r = __hmin2(*reinterpret_cast<__nv_bfloat162*>(&a),
-                             *reinterpret_cast<__nv_bfloat162*>(&b));
-  return *reinterpret_cast<uint32_t*>(&r);
-}
-__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
-  __nv_bfloat162 r = __hmax2(*reinterpret_cast<__nv_bfloat162*>(&a),
-                             *reinterpret_cast<__nv_bfloat162*>(&b));
-  return *reinterpret_cast<uint32_t*>(&r);
-}
-__device__ __forceinline__ uint2 vmin(uint2 a, uint2 b) {
-  return make_uint2(bmin2(a.x, b.x), bmin2(a.y, b.y));
-}
-__device__ __forceinline__ uint2 vmax(uint2 a, uint2 b) {
-  return make_uint2(bmax2(a.x, b.x), bmax2(a.y, b.y));
-}
-__device__ __forceinline__ uint32_t vmin(uint32_t a, uint32_t b) { return bmin2(a, b); }
-__device__ __forceinline__ uint32_t vmax(uint32_t a, uint32_t b) { return bmax2(a, b); }
-
 struct BulkParams {
   const uint16_t* k;
   uint16_t* summ;

@@ -107,9 +107,10 @@ class DecodeLoop:
     """
 
     def __init__(self, kvs, seq_lens0, q, k_new, v_new, gamma: float, budget: int = 0,
-                 sm_scale: float | None = None):
+                 sm_scale: float | None = None, fused_append: bool = True):
         """kvs: PagedKV per layer; seq_lens0: int32 [B] (T0); q: fp32 [n, L, B, Hq, d];
-        k_new, v_new: bf16 [n, L, B, Hkv, d]."""
+        k_new, v_new: bf16 [n, L, B, Hkv, d]. fused_append: append inside the score
+        pass (asp_coverage_select_append) instead of a separate APPEND launch."""
         kv0 = kvs[0]
         n, L = q.shape[0], len(kvs)
         assert q.shape == (n, L, kv0.batch, kv0.num_q_heads, kv0.head_dim)
@@ -130,23 +131,30 @@ class DecodeLoop:
                                dtype=torch.float32, device=dev)
         self.lse = torch.zeros((n, L, kv0.batch, kv0.num_q_heads), dtype=torch.float32,
                                device=dev)
+        self.fused_append = bool(fused_append)
         self.ws = B.new_workspace(kv0)
         self.graph = None
 
     @property
     def launches(self) -> int:
-        """Kernel launches of the whole loop: append, score, select, decode, merge."""
-        per = 2 if (self.budget > 0 or self.gamma < 1.0) else 1
-        return self.n * self.L * (1 + per + 2)
+        """Kernel launches of the whole loop: [append,] score, select, decode, merge."""
+        per = 2 if (self.budget > 0 or self.gamma < 1.0 or self.fused_append) else 1
+        return self.n * self.L * ((0 if self.fused_append else 1) + per + 2)
 
     def run(self, stream=None):
         for i in range(self.n):
             for l in range(self.L):
                 kv = self.kvs[i][l]
-                B.asp_page_summarize(kv, B.ASP_SUMMARIZE_APPEND, self.k_new[i, l],
-                                     self.v_new[i, l], self.ws, stream)
-                B.asp_coverage_select(kv, self.q[i, l], self.gamma, self.budget,
-                                      self.lists[i, l], self.lens[i, l], self.ws, stream)
+                if self.fused_append:
+                    B.asp_coverage_select_append(kv, self.k_new[i, l], self.v_new[i, l],
+                                                 self.q[i, l], self.gamma, self.budget,
+                                                 self.lists[i, l], self.lens[i, l], self.ws,
+                                                 stream)
+                else:
+                    B.asp_page_summarize(kv, B.ASP_SUMMARIZE_APPEND, self.k_new[i, l],
+                                         self.v_new[i, l], self.ws, stream)
+                    B.asp_coverage_select(kv, self.q[i, l], self.gamma, self.budget,
+                                          self.lists[i, l], self.lens[i, l], self.ws, stream)
                 B.asp_sparse_decode(kv, self.q[i, l], self.lists[i, l], self.lens[i, l],
                                     self.sm_scale, self.out[i, l], self.lse[i, l], self.ws,
                                     stream)

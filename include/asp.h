@@ -177,6 +177,23 @@ asp_status asp_coverage_select(const asp_paged_kv* kv, const float* q, float gam
                                void* ws, size_t ws_bytes, asp_stream stream);
 
 /*
+ * APPEND and coverage selection in one pass: the same result as
+ * asp_page_summarize(kv, ASP_SUMMARIZE_APPEND, k_new, v_new, ...) followed by
+ * asp_coverage_select(kv, q, gamma, budget, lists, lens, ...), with the
+ * append done inside the score kernel (no separate launch per layer and
+ * step). The score kernel's warp that streams a segment's last page first
+ * writes the new token's K and V rows into slot (T_b-1) % P of page
+ * (T_b-1) / P and folds the key into that page's summary, then reads it.
+ * k_new, v_new : bf16 [B, Hkv, d], 16-byte aligned. seq_lens already count
+ * the new token; requests with T_b == 0 are skipped. Idempotent, like APPEND.
+ * Errors and outputs as for the two calls it replaces.
+ */
+asp_status asp_coverage_select_append(const asp_paged_kv* kv, const uint16_t* k_new,
+                                      const uint16_t* v_new, const float* q, float gamma,
+                                      int32_t budget, int32_t* lists, int32_t* lens, void* ws,
+                                      size_t ws_bytes, asp_stream stream);
+
+/*
  * Page scores alone: the estimate that asp_coverage_select ranks (MOIRA
  * abstract: "estimated attention mass" per page; the Quest bound as named in
  * the HiSparse abstract), for diagnostics such as the captured mass of a

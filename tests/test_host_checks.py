@@ -65,6 +65,12 @@ def test_null_outputs_and_modes(lib):
     assert lib.asp_page_summarize(ctypes.byref(s), 1, None, None, FAKE, 1, None) == B.ASP_EINVAL
     assert lib.asp_page_summarize(ctypes.byref(s), 0, FAKE, FAKE, FAKE, 1, None) == B.ASP_EINVAL
     assert lib.asp_page_scores(ctypes.byref(s), None, FAKE, FAKE, 1, None) == B.ASP_EINVAL
+    assert lib.asp_coverage_select_append(ctypes.byref(s), None, FAKE, FAKE, 0.9, 0, FAKE, FAKE,
+                                          FAKE, 1, None) == B.ASP_EINVAL
+    assert lib.asp_coverage_select_append(ctypes.byref(s), FAKE, FAKE + 8, FAKE, 0.9, 0, FAKE,
+                                          FAKE, FAKE, 1, None) == B.ASP_EINVAL
+    assert lib.asp_coverage_select_append(ctypes.byref(s), FAKE, FAKE, FAKE, 0.0, 0, FAKE, FAKE,
+                                          FAKE, 1, None) == B.ASP_EINVAL
     assert lib.asp_page_scores(ctypes.byref(s), FAKE, None, FAKE, 1, None) == B.ASP_EINVAL
     assert lib.asp_page_scores(ctypes.byref(s), FAKE + 4, FAKE, FAKE, 1, None) == B.ASP_EINVAL
 

@@ -39,7 +39,7 @@ def _worker(rank, world, port, out):
 
 def test_two_ranks_gloo():
     world, port = 2, _free_port()
-    mgr = tmp.Manager()
+    mgr = tmp.get_context("spawn").Manager()
     out = mgr.dict()
     tmp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
     assert out[0][0] == out[1][0] == 1.5          # max over ranks on every rank
