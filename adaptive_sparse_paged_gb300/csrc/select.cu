@@ -108,7 +108,7 @@ struct SegCursor {
   int b, h, lp, pos;
 };
 
-template <int D, int G>
+template <int D, int G, bool Append>
 __global__ void __launch_bounds__(kScoreThreads, ScoreCfg<D, G>::kCtas)
     score_kernel(ScoreParams p) {
   using C = ScoreCfg<D, G>;
@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(kScoreThreads, ScoreCfg<D, G>::kCtas)
       int n = 0;
       if (b < p.B) {
         const int T = clamp_seq_len(p.seq_lens[b], p.max_pages, p.P, p.err);
-        tlen[b] = T;
+        if (Append) tlen[b] = T;
         n = ceil_div(T, p.P);
       }
       int x = n;
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kScoreThreads, ScoreCfg<D, G>::kCtas)
   auto issue = [&]() {  // next piece of the slice into slot issued % kSlots
     const int n = piece_pages(ic);
     const int slot = issued % kSlots;
-    const bool app = p.k_new != nullptr && ic.lp + n == seg_pages(ic.b);  // warp-uniform
+    const bool app = Append && ic.lp + n == seg_pages(ic.b);  // warp-uniform
     if (app) append_token(ic.b, ic.h, ic.lp + n - 1);
     if (lane == 0) mbar_arrive_expect_tx(&full[slot], n * kPageBytes);
     __syncwarp();
@@ -1042,8 +1042,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
   if (tid == 0) p.lens[s] = (int32_t)(above_c + t);
 }
 
-template <int D, int G>
-cudaError_t launch_score_t(const SelectArgs& a, cudaStream_t stream) {
+template <int D, int G, bool Append>
+cudaError_t launch_score_tt(const SelectArgs& a, cudaStream_t stream) {
   const asp_paged_kv& kv = *a.kv;
   ScoreParams p{kv.summaries, a.q, kv.seq_lens, a.scores, a.err, kv.batch, kv.num_q_heads,
                 kv.num_kv_heads, kv.page_size, kv.max_pages, 1.0f / sqrtf((float)D),
@@ -1051,11 +1051,16 @@ cudaError_t launch_score_t(const SelectArgs& a, cudaStream_t stream) {
   using C = ScoreCfg<D, G>;
   const size_t smem = (size_t)kScoreWarps * C::kSlots * (C::kSlotBytes + sizeof(uint64_t)) +
                       (2 * kv.batch + 1) * sizeof(int);
-  cudaError_t e = set_max_dynamic_smem((const void*)score_kernel<D, G>, (int)smem);
+  cudaError_t e = set_max_dynamic_smem((const void*)score_kernel<D, G, Append>, (int)smem);
   if (e != cudaSuccess) return e;
   // persistent: the kernel splits the pages it finds in seq_lens itself
-  return launch_pdl(score_kernel<D, G>, dim3(C::kCtas * a.num_sms), dim3(kScoreThreads), smem,
-                    stream, p);
+  return launch_pdl(score_kernel<D, G, Append>, dim3(C::kCtas * a.num_sms), dim3(kScoreThreads),
+                    smem, stream, p);
+}
+
+template <int D, int G>
+cudaError_t launch_score_t(const SelectArgs& a, cudaStream_t stream) {
+  return a.k_new ? launch_score_tt<D, G, true>(a, stream) : launch_score_tt<D, G, false>(a, stream);
 }
 
 template <int D>

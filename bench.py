@@ -374,7 +374,7 @@ def run_asp(args):
             B.asp_page_summarize(kv, B.ASP_SUMMARIZE_BULK, None, None, ws0)
         steps_in = synth.make_steps(w, [lay.q for lay in layers], n_ms, seed, dev)
         loop = DecodeLoop(kvs, t0.clone(), steps_in.q, steps_in.k_new, steps_in.v_new,
-                          gamma=args.gamma)
+                          gamma=args.gamma)  # append fused into the score pass
         loop.capture()
         loop.replay()  # the first run: fresh steps
         torch.cuda.synchronize()
@@ -382,16 +382,25 @@ def run_asp(args):
         lens_ms = loop.lens.cpu().numpy().astype(np.int64)  # [n, L, B, Hkv]
         Km = max(3, args.steps // 20)
         t_ms = max_over_ranks(timed_graph(loop, Km, 3), dist, dev)
+        launches_ms = loop.launches
+        del loop
+        # the same loop with the append as its own kernel, for comparison
+        sep = DecodeLoop(kvs, t0.clone(), steps_in.q, steps_in.k_new, steps_in.v_new,
+                         gamma=args.gamma, fused_append=False)
+        sep.capture()
+        t_sep = max_over_ranks(timed_graph(sep, Km, 3), dist, dev)
+        del sep
         sh.seq_lens.copy_(full_lens)  # the appended tokens are now the context's last ones
         torch.cuda.synchronize()
         tpot = t_ms / (Km * n_ms)
         frac = [round(float(lens_ms[i].sum()) / all_pages, 4) for i in range(n_ms)]
-        multi = {"steps_in_graph": n_ms, "append": True, "tpot_ms": round(1e3 * tpot, 4),
-                 "steps_per_s": round(world / tpot, 3), "replays": Km,
-                 "pages_read_frac_by_step": frac,
-                 "launches_per_graph": loop.launches,
+        multi = {"steps_in_graph": n_ms, "append": "fused into the score pass",
+                 "tpot_ms": round(1e3 * tpot, 4), "steps_per_s": round(world / tpot, 3),
+                 "tpot_ms_append_separate": round(1e3 * t_sep / (Km * n_ms), 4),
+                 "replays": Km, "pages_read_frac_by_step": frac,
+                 "launches_per_graph": launches_ms,
                  "query_change": "per step: layer queries + 0.25 * N(0, 1)"}
-        del loop, steps_in
+        del steps_in
 
     cpu = None
     if pool is not None:
