@@ -426,8 +426,8 @@ __device__ __forceinline__ void block_minmax(float& mn, float& mx, float* scratc
     scratch[kSelWarps + warp] = mx;
   }
   __syncthreads();
-  mn = scratch[lane];
-  mx = scratch[kSelWarps + lane];
+  mn = lane < kSelWarps ? scratch[lane] : INFINITY;
+  mx = lane < kSelWarps ? scratch[kSelWarps + lane] : -INFINITY;
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) {
     mn = fminf(mn, __shfl_xor_sync(kFull, mn, o));
@@ -583,8 +583,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
     }
     __syncthreads();
     if (warp == 0) {
-      const unsigned long long w0 = red_u64[lane];
-      const uint32_t c0 = red_u32[lane];
+      const unsigned long long w0 = lane < kSelWarps ? red_u64[lane] : 0ull;
+      const uint32_t c0 = lane < kSelWarps ? red_u32[lane] : 0u;
       unsigned long long aw = w0;
       uint32_t ac = c0;
 #pragma unroll
@@ -596,8 +596,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
           ac += yc;
         }
       }
-      red_u64[lane] = aw - w0;  // exclusive warp offsets
-      red_u32[lane] = ac - c0;
+      if (lane < kSelWarps) {
+        red_u64[lane] = aw - w0;  // exclusive warp offsets
+        red_u32[lane] = ac - c0;
+      }
       if (lane == 31) {  // gamma times the total weight, once (fp64 is slow on this part)
         unsigned long long tg = target;
         if (mass_mode) {
@@ -882,8 +884,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
         red_u32[kSelWarps + warp] = kmax;
       }
       __syncthreads();
-      kmin = red_u32[lane];
-      kmax = red_u32[kSelWarps + lane];
+      kmin = lane < kSelWarps ? red_u32[lane] : 0xffffffffu;
+      kmax = lane < kSelWarps ? red_u32[kSelWarps + lane] : 0u;
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) {
         kmin = min(kmin, __shfl_xor_sync(kFull, kmin, o));
@@ -981,8 +983,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
       red_u32[kSelWarps + warp] = kmax;
     }
     __syncthreads();
-    kmin = red_u32[lane];
-    kmax = red_u32[kSelWarps + lane];
+    kmin = lane < kSelWarps ? red_u32[lane] : 0xffffffffu;
+    kmax = lane < kSelWarps ? red_u32[kSelWarps + lane] : 0u;
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) {
       kmin = min(kmin, __shfl_xor_sync(kFull, kmin, o));
@@ -1017,13 +1019,13 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
   if (lane == 31) red_u64[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    unsigned long long w = red_u64[lane], xx = w;
+    unsigned long long w = lane < kSelWarps ? red_u64[lane] : 0ull, xx = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const unsigned long long y = __shfl_up_sync(kFull, xx, o);
       if (lane >= o) xx += y;
     }
-    red_u64[lane] = xx - w;  // exclusive warp offsets
+    if (lane < kSelWarps) red_u64[lane] = xx - w;  // exclusive warp offsets
   }
   __syncthreads();
   const unsigned long long pre = red_u64[warp] + x - pv;
