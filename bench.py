@@ -355,6 +355,26 @@ def run_asp(args):
            "h2d_bytes_per_step": int(q_host.numel() * 4),
            "d2h_bytes_per_step": int(out_host.numel() * 4 + lse_host.numel() * 4)}
 
+    # the same step at the pages' own sparsity: the top 30% of pages by score
+    # (budget mode), so the fixed per-layer costs weigh as they would there
+    at30 = None
+    if not args.no_dense:
+        k30 = int(math.ceil(0.3 * float(n_pages.max())))
+        bstep = DecodeStep(kvs, q_all, gamma=args.gamma, budget=k30)
+        bstep.capture()
+        Kb = max(3, args.steps // 4)
+        tb = max_over_ranks(timed_graph(bstep, Kb, 3), dist, dev)
+        blens = bstep.lens.cpu().numpy().astype(np.int64)
+        b_dec = sum(int(blens[l].sum()) * (page_bytes + 8) + q_bytes + Bt * Hkv * 4 + out_bytes
+                    for l in range(L))
+        b_sel = sum(int(n_pages.sum()) * Hkv * 4 + int(blens[l].sum()) * 4 + Bt * Hkv * 4
+                    for l in range(L))
+        b_bytes = b_dec + L * score_bytes + b_sel
+        at30 = {"budget_pages": k30, "pages_read_frac": round(float(blens.sum()) / all_pages, 4),
+                "steps_per_s": round(world * Kb / tb, 3), "ms_per_step": round(1e3 * tb / Kb, 4),
+                "hbm_frac_of_measured": round(b_bytes / (tb / Kb) / 1e9 / peak, 4)}
+        del bstep
+
     # required page fractions per gamma, and a fixed budget of equal bytes
     diag = None
     if not args.no_diagnostics:
@@ -454,6 +474,7 @@ def run_asp(args):
             "selected_page_heads_per_step": sel_pages,
             "bytes_per_step": step_bytes,
             "dense_gamma1": dense,
+            "top30_budget": at30,
             "multi_step": multi,
             "budget_diagnostics": diag,
             "kernels_ms": {"select_avg": round(sel_avg_s * 1e3, 4),
