@@ -436,6 +436,10 @@ __device__ __forceinline__ void block_minmax(float& mn, float& mx, float* scratc
   __syncthreads();  // scratch is free again
 }
 
+// General = false: every segment fits the fast path (max_pages <= kSelCache,
+// known on the host), so the general path is compiled out and the kernel's
+// code, fetched afresh on every SM at each launch, is smaller.
+template <bool General>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
   extern __shared__ __align__(16) uint8_t sel_smem[];
   uint32_t* hist = reinterpret_cast<uint32_t*>(sel_smem);  // [warp][bin][count, l0, l1, l2]
@@ -471,7 +475,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
   const float* gsc = p.scores + (size_t)s * p.max_pages;
   // fast path: element k of this thread is page id k * kSelThreads + tid, so a
   // warp's elements of one slab k are 32 consecutive ids
-  const bool fast = N <= kSelCache;
+  const bool fast = !General || N <= kSelCache;
   float v[kPer];
   float lo_s = INFINITY, hi_s = -INFINITY;
   if (fast) {
@@ -1091,10 +1095,13 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream) {
   }
   SelectParams p{a.scores, kv.seq_lens, a.lists, a.lens, a.err, kv.num_kv_heads, kv.page_size,
                  kv.max_pages, a.gamma, a.budget};
-  cudaError_t e = set_max_dynamic_smem((const void*)select_kernel, (int)kSelSmem);
+  const bool general = kv.max_pages > kSelCache;
+  const void* fn = general ? (const void*)select_kernel<true> : (const void*)select_kernel<false>;
+  cudaError_t e = set_max_dynamic_smem(fn, (int)kSelSmem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(select_kernel, dim3(kv.batch * kv.num_kv_heads), dim3(kSelThreads), kSelSmem,
-                    stream, p);
+  const dim3 grid(kv.batch * kv.num_kv_heads);
+  return general ? launch_pdl(select_kernel<true>, grid, dim3(kSelThreads), kSelSmem, stream, p)
+                 : launch_pdl(select_kernel<false>, grid, dim3(kSelThreads), kSelSmem, stream, p);
 }
 
 }  // namespace asp
