@@ -19,16 +19,22 @@
 //                the block table runs at under half the copy bandwidth;
 //                contiguous runs reach it.)
 //
-// select_kernel  One CTA per segment. Softmax weights exp(s - max) are turned
-//                into fixed point (2^38 = weight of the top page), so every
-//                sum is exact and order-independent. A radix select over
-//                order-preserving score keys, with histograms of count and
-//                mass over the candidates' actual key range, finds the cutoff
-//                score in at most four rounds; ties at the cutoff go to the
-//                lower page ids; one block scan compacts the kept ids in
-//                ascending order. Each warp fills a private histogram of
-//                32-bit words (a mass is three 13-bit limbs, so no word can
-//                overflow), which keeps hot bins from serialising the CTA.
+// select_kernel  One CTA (1024 threads) per segment. Softmax weights
+//                exp(s - max) are turned into fixed point (2^37 = weight of
+//                the top page), so every sum is exact and order-independent
+//                and the result is deterministic. A first pass histograms
+//                the weights over 4096 bins linear in max - s; the bin where
+//                the running weight from the top reaches gamma times the
+//                total is one interval of score keys, usually a handful of
+//                pages, which one warp resolves exactly (exact radix rounds
+//                over the keys when many pages tie closely). Ties at the
+//                cutoff go to the lower page ids; per-warp ballots and one
+//                scan compact the kept ids in ascending order. Segments of
+//                up to 8192 pages keep scores and weights in registers;
+//                longer ones read them from global memory (that general path
+//                is compiled out of the variant launched when max_pages is
+//                at most 8192).
+
 #include "asp_internal.cuh"
 
 #include <type_traits>
