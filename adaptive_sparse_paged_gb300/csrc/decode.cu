@@ -7,10 +7,10 @@
 // take their inclusive prefix; the concatenated lists form one sequence of
 // `total` pages, split evenly over the G CTAs (the first total % G take one
 // position more), so shares differ by at most one page whatever the length
-// mix. A CTA's range cuts at most two segments; each (segment, CTA) piece produces one partial
-// (m, l, o) in slot segment + CTA of the workspace, which is unique because
-// both indices grow along the sequence; a segment held whole by one CTA is
-// written out directly. A small second kernel merges the split segments by
+// mix. A CTA's range cuts at most two segments; each (segment, CTA) piece
+// produces one partial (m, l, o) in slot segment + CTA of the workspace,
+// which is unique because both indices grow along the sequence; a segment
+// held whole by one CTA is written out directly. A small second kernel merges the split segments by
 // log-sum-exp. The streaming kernel thus never fences, counts or waits on
 // another CTA: under full HBM load each such round trip costs 1.5-2 us, and
 // at a piece end it would stall that CTA's copy pipeline.
@@ -34,7 +34,8 @@
 // The S^T accumulator becomes the P^T operand through movmatrix.trans, and the
 // swizzled tiles make every ldmatrix conflict-free. A page is 4-32 KiB of HBM
 // against 4-8 flop per byte, far below any tensor-core limit: the kernel is
-// bound by HBM, and the 128 KiB ring keeps that much per SM in flight.
+// bound by HBM, and the ring (128 KiB, or 192 KiB when the segment prefix
+// leaves room in shared memory) keeps that much per SM in flight.
 #include "asp_internal.cuh"
 
 #include <cudaTypedefs.h>
