@@ -301,3 +301,27 @@ def test_device_error_on_bad_page(cuda_device):
     case.sh.block_table.copy_(synth.make_shared(w, 8, cuda_device).block_table)
     res = case.run(0, 0.9)
     check_case(case, 0, 0.9, 0, *res)
+
+
+def test_maximum_segment_count(cuda_device):
+    """4096 segments (512 requests x 8 KV heads), the most one call accepts.
+
+    The decode's per-CTA prefix of list lengths then takes 16 KiB of shared
+    memory, which leaves the regular (two-slot) ring; the select grid has 4096
+    CTAs and the score kernel's request prefix 512 entries. Lengths are drawn
+    from 0 to 400 tokens (empty requests and partial pages included); 300
+    seeded segments are checked against the oracle, every length for range.
+    """
+    rng = np.random.default_rng(41)
+    lens = [int(x) for x in rng.integers(0, 401, size=512)]
+    lens[:3] = [0, 1, 16]
+    w = small("max_segments", 512, 32, 8, 64, 16, 1)
+    case = Case(w, seed=41, device=cuda_device, seq_lens=lens)
+    res = case.run(0, 0.9)
+    n_pages = np.array(case.sh.num_pages)
+    ln = res[1].cpu().numpy()
+    assert np.all(ln >= 0) and np.all(ln <= n_pages[:, None])
+    assert np.all((ln == 0) == (n_pages[:, None] == 0))
+    segs = [(int(b), int(h)) for b, h in zip(rng.integers(0, 512, 300), rng.integers(0, 8, 300))]
+    segs += [(0, 0), (1, 3), (2, 7)]
+    check_case(case, 0, 0.9, 0, *res, segs=segs)
