@@ -835,6 +835,23 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
     return t;
   };
 
+  // Mass mode, fast path: the tie count before its clamp to [1, n_eq],
+  // ceil((target - above_w) / w(tau)), computed by one thread as soon as tau
+  // is known so that it stays off the compaction's critical path. Counts
+  // from 2^22 up exceed every n_eq (at most 2^20) and need no refinement;
+  // below that the float estimate is within one of the exact value.
+  auto tie_mass = [&](uint32_t tau, unsigned long long above_w) -> unsigned long long {
+    const unsigned long long w = mass_fixed(key_score(tau), smax);
+    if (!w) return 1ull << 40;  // ties of zero mass: all of them
+    const unsigned long long rem = target - above_w;
+    const float est = ceilf((float)rem / (float)w);
+    if (est >= 4194304.0f) return 1ull << 40;
+    unsigned long long t = (unsigned long long)est;
+    while (t * w < rem) ++t;
+    while (t > 1 && (t - 1) * w >= rem) --t;
+    return t;
+  };
+
   if (fast) {
     // candidates of the cutoff bin (weights recomputed from the scores)
     float* cand = reinterpret_cast<float*>(hist + kBins * 4);
@@ -869,6 +886,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
         if (lane == __ffs(at) - 1) {
           pick[0] = best;
           pick_m[0] = above_m + gt_w;
+          if (mass_mode) tie_t = tie_mass(best, above_m + gt_w);
         }
       }
       __syncthreads();
@@ -906,6 +924,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
       cnt_eq = nc;
       __syncthreads();
       radix_resolve();
+      if (tid == 0 && mass_mode) tie_t = tie_mass(lo, above_m);
     }
     const uint32_t tau = lo;
     // compaction in id order: per (slab, warp) counts of keys above and at
@@ -953,7 +972,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
       }
       if (lane == 31) {
         pick[1] = xg;  // keys above tau
-        tie_t = tie_take(tau, mass_mode ? above_m : xg, xe);
+        const unsigned long long t0 = mass_mode ? tie_t : target - xg;
+        tie_t = t0 < 1 ? 1 : (t0 > xe ? (unsigned long long)xe : t0);
       }
     }
     __syncthreads();
