@@ -165,6 +165,12 @@ class ClockSampler:
                                     if r[4].replace(".", "").isdigit()), default=None)}
 
 
+def workload_name(w, gamma) -> str:
+    """The workload both arms report in config.workload."""
+    return (f"{w.name}: B{w.batch} L{w.layers} Hq{w.num_q_heads} Hkv{w.num_kv_heads} "
+            f"d{w.head_dim} P{w.page_size} T{w.seq_len or 'lognormal'} gamma{gamma}")
+
+
 # ------------------------------------------------------------- oracle sample
 def _oracle_worker(args):
     import numpy as np
@@ -458,8 +464,8 @@ def run_asp(args):
             "dtype": "bf16",
             "data": "synthetic",
             "config": {
-                "workload": f"{w.name}: B{w.batch} L{w.layers} Hq{Hq} Hkv{Hkv} d{d} P{P} "
-                            f"T{w.seq_len or 'lognormal'} gamma{args.gamma}, one CUDA graph per step",
+                "workload": workload_name(w, args.gamma),
+                "step": "all layers replayed from one CUDA graph",
                 "gamma": args.gamma,
                 "l2": "inputs larger than L2 (K/V %.1f GiB, summaries %.2f GiB resident); no flush"
                       % (2 * sh.num_phys_pages * Hkv * P * d * 2 * L / 2**30,
@@ -529,10 +535,8 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": f"{w.name}: B{w.batch} L{w.layers} Hq{w.num_q_heads} "
-                               f"Hkv{w.num_kv_heads} d{w.head_dim} P{w.page_size} "
-                               f"T{w.seq_len or 'lognormal'} gamma{args.gamma}",
-                   "gamma": args.gamma},
+        "config": {"workload": workload_name(w, args.gamma), "gamma": args.gamma,
+                   "step": "fp64 oracle on the host cores, bounded sample per step"},
         "cpu_baseline": {"value": value, "unit": "steps/s", "cores": cores, "kind": "oracle",
                          "sample": f"each step: {len(tasks)} of {segs_per_step} segments of "
                                    f"layer 0 through the fp64 oracle, scaled to a full step"},
