@@ -74,7 +74,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
             raise RuntimeError("nvcc failed on: " + ", ".join(failed))
         out_tmp = os.path.join(tmp, "libasp.so")
         link = [nvcc, "-shared", "-o", out_tmp] + objs + ARCH + [
-            "-cudart", "shared", "-Xlinker", "-rpath," + _cuda_lib_dir(nvcc)]
+            "-cudart", "shared", "-ldl", "-Xlinker", "-rpath," + _cuda_lib_dir(nvcc)]
         if verbose:
             print(" ".join(link), flush=True)
         r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)

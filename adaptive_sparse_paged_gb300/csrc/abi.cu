@@ -131,6 +131,7 @@ asp_status asp_workspace_init(void* ws, size_t ws_bytes, asp_stream stream) {
 asp_status asp_page_summarize(const asp_paged_kv* kv, int32_t mode, const uint16_t* k_new,
                               const uint16_t* v_new, void* ws, size_t ws_bytes,
                               asp_stream stream) {
+  NvtxRange range("asp_page_summarize");
   asp_status st = check_kv(kv);
   if (st != ASP_OK) return st;
   if (mode == ASP_SUMMARIZE_BULK) {
@@ -151,6 +152,7 @@ asp_status asp_page_summarize(const asp_paged_kv* kv, int32_t mode, const uint16
 asp_status asp_coverage_select(const asp_paged_kv* kv, const float* q, float gamma,
                                int32_t budget, int32_t* lists, int32_t* lens, void* ws,
                                size_t ws_bytes, asp_stream stream) {
+  NvtxRange range("asp_coverage_select");
   asp_status st = check_kv(kv);
   if (st != ASP_OK) return st;
   if (!q || !lists || !lens) return ASP_EINVAL;
@@ -169,6 +171,7 @@ asp_status asp_coverage_select_append(const asp_paged_kv* kv, const uint16_t* k_
                                       const uint16_t* v_new, const float* q, float gamma,
                                       int32_t budget, int32_t* lists, int32_t* lens, void* ws,
                                       size_t ws_bytes, asp_stream stream) {
+  NvtxRange range("asp_coverage_select_append");
   asp_status st = check_kv(kv);
   if (st != ASP_OK) return st;
   if (!q || !lists || !lens || !k_new || !v_new) return ASP_EINVAL;
@@ -187,6 +190,7 @@ asp_status asp_coverage_select_append(const asp_paged_kv* kv, const uint16_t* k_
 
 asp_status asp_page_scores(const asp_paged_kv* kv, const float* q, float* scores, void* ws,
                            size_t ws_bytes, asp_stream stream) {
+  NvtxRange range("asp_page_scores");
   asp_status st = check_kv(kv);
   if (st != ASP_OK) return st;
   if (!q || !scores) return ASP_EINVAL;
@@ -202,6 +206,7 @@ asp_status asp_page_scores(const asp_paged_kv* kv, const float* q, float* scores
 asp_status asp_sparse_decode(const asp_paged_kv* kv, const float* q, const int32_t* lists,
                              const int32_t* lens, float sm_scale, float* out, float* lse,
                              void* ws, size_t ws_bytes, asp_stream stream) {
+  NvtxRange range("asp_sparse_decode");
   asp_status st = check_kv(kv);
   if (st != ASP_OK) return st;
   if (!q || !lists || !lens || !out || !lse) return ASP_EINVAL;

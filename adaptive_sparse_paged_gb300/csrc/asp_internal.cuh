@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cstddef>
 #include <cstdint>
@@ -13,6 +14,17 @@
 #include "asp.h"
 
 namespace asp {
+
+// Named NVTX range over one host entry point, so a profiler that reads NVTX
+// (Nsight Systems, or ncu with --nvtx and --nvtx-include) attributes the
+// kernels a call launches to that call. With no tool attached, push and pop
+// only test a null hook.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 constexpr int kMaxSegments = 4096;     // batch * Hkv handled by one call
 constexpr int kMaxPages = 1 << 20;     // max_pages bound (int32 page-space arithmetic)

@@ -57,6 +57,7 @@ extern "C" asp_status asp_coverage_select_noalloc(const asp_paged_kv* kv, const 
                                                   int32_t* lens, uint32_t* dev_error,
                                                   asp_stream stream) {
   using namespace asp;
+  NvtxRange range("asp_coverage_select_noalloc");
   if (!kv || !q || !lists || !lens) return ASP_EINVAL;
   // the capacity limit comes first, before anything touches the device
   if (kv->batch > 0 && kv->num_kv_heads > 0 && kv->max_pages > 0 &&

@@ -18,3 +18,12 @@ def cuda_device():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     return torch.device("cuda", 0)
+
+
+@pytest.fixture(autouse=True)
+def _guard_bands():
+    """Checks, when each test ends, the guard bands its buffers were given."""
+    yield
+    from tests import guards
+    if guards.registered():
+        guards.check_guards()

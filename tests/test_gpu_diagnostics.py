@@ -12,6 +12,7 @@ import torch
 
 from adaptive_sparse_paged_gb300 import binding as B
 from adaptive_sparse_paged_gb300 import diagnostics as Dg
+from tests import guards
 from tests.test_gpu_parity import Case, small
 
 pytestmark = pytest.mark.gpu
@@ -29,10 +30,12 @@ def test_budget_diagnostics_properties(cuda_device):
     assert fb["pages_per_segment"] >= 1 and 0 < fb["captured_mass"]["mean"] <= 1 + 1e-9
     # the coverage rule's own lists reach gamma of the estimated mass, minimally
     kv, q = case.kvs[0], case.layers[0].q
-    lists = torch.zeros((w.batch, w.num_kv_heads, case.sh.max_pages), dtype=torch.int32,
-                        device=cuda_device)
-    lens = torch.zeros((w.batch, w.num_kv_heads), dtype=torch.int32, device=cuda_device)
-    scores = torch.zeros((w.batch, w.num_kv_heads, case.sh.max_pages), device=cuda_device)
+    lists = guards.guarded((w.batch, w.num_kv_heads, case.sh.max_pages), torch.int32,
+                           cuda_device, fill=0, what="lists")
+    lens = guards.guarded((w.batch, w.num_kv_heads), torch.int32, cuda_device, fill=0,
+                          what="lens")
+    scores = guards.guarded((w.batch, w.num_kv_heads, case.sh.max_pages), torch.float32,
+                            cuda_device, fill=0, what="scores")
     B.asp_coverage_select(kv, q, 0.99, 0, lists, lens, case.ws)
     B.asp_page_scores(kv, q, scores, case.ws)
     assert B.asp_get_device_error(case.ws) == 0

@@ -15,6 +15,7 @@ import torch
 
 from adaptive_sparse_paged_gb300 import binding as B
 from adaptive_sparse_paged_gb300 import synth
+from tests import guards
 from tests.test_gpu_parity import Case, small
 
 pytestmark = pytest.mark.gpu
@@ -51,9 +52,9 @@ def test_fused_append_equals_separate_calls(cuda_device, d, P, g, lens, gamma, b
     outs = []
     for c, fused in ((a, False), (b, True)):
         kv, q = c.kvs[0], c.layers[0].q
-        lists = torch.full((w.batch, Hkv, c.sh.max_pages), -3, dtype=torch.int32,
-                           device=cuda_device)
-        ln = torch.full((w.batch, Hkv), -3, dtype=torch.int32, device=cuda_device)
+        lists = guards.guarded((w.batch, Hkv, c.sh.max_pages), torch.int32, cuda_device,
+                               fill=-3, what="lists")
+        ln = guards.guarded((w.batch, Hkv), torch.int32, cuda_device, fill=-3, what="lens")
         for _ in range(2):  # idempotent: a second pass changes nothing
             if fused:
                 B.asp_coverage_select_append(kv, k_new, v_new, q, gamma, budget, lists, ln, c.ws)

@@ -25,7 +25,7 @@ from adaptive_sparse_paged_gb300 import binding as B
 from adaptive_sparse_paged_gb300 import synth
 from adaptive_sparse_paged_gb300.step import DecodeLoop
 from tests import parity
-from tests.test_gpu_parity import Case, small
+from tests.test_gpu_parity import Case, guard_outputs, small
 
 pytestmark = pytest.mark.gpu
 
@@ -47,6 +47,7 @@ def test_decode_loop_matches_oracle(cuda_device, gamma, budget):
     steps = synth.make_steps(w, [lay.q for lay in case.layers], n, seed=6, device=cuda_device)
     loop = DecodeLoop(case.kvs, case.sh.seq_lens.clone(), steps.q, steps.k_new, steps.v_new,
                       gamma, budget)
+    guard_outputs(loop)
     loop.capture()
     loop.replay()  # the first launch of the loop: fresh steps
     torch.cuda.synchronize()
@@ -107,6 +108,7 @@ def test_decode_loop_replay_is_stable(cuda_device):
     steps = synth.make_steps(w, [case.layers[0].q], n, seed=10, device=cuda_device)
     loop = DecodeLoop(case.kvs, case.sh.seq_lens.clone(), steps.q, steps.k_new, steps.v_new,
                       0.9)
+    guard_outputs(loop)
     loop.capture()
     loop.replay()
     torch.cuda.synchronize()

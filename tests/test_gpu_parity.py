@@ -17,14 +17,31 @@ import oracle.asp_oracle as O
 from adaptive_sparse_paged_gb300 import binding as B
 from adaptive_sparse_paged_gb300 import synth
 from adaptive_sparse_paged_gb300.step import DecodeStep
-from tests import parity
+from tests import guards, parity
 
 pytestmark = pytest.mark.gpu
 
 
 # ------------------------------------------------------------------ fixtures
+GUARD_CACHE_BYTES = 256 << 20  # K/V caches up to this size get guard bands too
+
+
+def guard_outputs(step):
+    """Moves a DecodeStep's or DecodeLoop's outputs and workspace into guarded buffers."""
+    for name in ("lists", "lens", "out", "lse"):
+        t = getattr(step, name)
+        setattr(step, name, guards.guarded(t.shape, t.dtype, t.device, fill=0, what=name))
+    step.ws = guards.guarded_workspace(step.kvs[0] if not isinstance(step.kvs[0], list)
+                                       else step.kvs[0][0])
+
+
 class Case:
-    """A workload built on the GPU: shared tables, layers, PagedKVs (BULK-summarised)."""
+    """A workload built on the GPU: shared tables, layers, PagedKVs (BULK-summarised).
+
+    Every buffer a kernel writes (summaries, workspace, outputs, and the K/V
+    caches of small cases, which APPEND writes) sits between guard bands that
+    tests/conftest.py checks when the test ends.
+    """
 
     def __init__(self, w: synth.Workload, seed: int, device, seq_lens=None, max_pages=None,
                  layers=None):
@@ -34,12 +51,16 @@ class Case:
         self.layers, self.kvs = [], []
         for l in self.layer_ids:
             lay = synth.make_layer(w, self.sh, seed, l, device)
-            summ = B.new_summaries(lay.k_cache, self.sh.block_table)
+            if lay.k_cache.numel() * 2 <= GUARD_CACHE_BYTES:
+                lay.k_cache = guards.guarded_like(lay.k_cache, what=f"k_cache[{l}]")
+                lay.v_cache = guards.guarded_like(lay.v_cache, what=f"v_cache[{l}]")
+            summ = guards.guarded((w.batch, w.num_kv_heads, self.sh.max_pages, 2, w.head_dim),
+                                  torch.bfloat16, device, fill=0, what=f"summaries[{l}]")
             kv = B.PagedKV(lay.k_cache, lay.v_cache, summ, self.sh.block_table, self.sh.seq_lens,
                            w.num_q_heads)
             self.layers.append(lay)
             self.kvs.append(kv)
-        self.ws = B.new_workspace(self.kvs[0])
+        self.ws = guards.guarded_workspace(self.kvs[0])
         for kv in self.kvs:
             B.asp_page_summarize(kv, B.ASP_SUMMARIZE_BULK, None, None, self.ws)
         assert B.asp_get_device_error(self.ws) == 0
@@ -51,11 +72,14 @@ class Case:
     def run(self, i, gamma, budget=0):
         kv, lay = self.kvs[i], self.layers[i]
         w = self.w
-        lists = torch.full((w.batch, w.num_kv_heads, self.sh.max_pages), -7, dtype=torch.int32,
-                           device=kv.device)
-        lens = torch.full((w.batch, w.num_kv_heads), -7, dtype=torch.int32, device=kv.device)
-        out = torch.full((w.batch, w.num_q_heads, w.head_dim), float("nan"), device=kv.device)
-        lse = torch.full((w.batch, w.num_q_heads), float("nan"), device=kv.device)
+        dev = kv.device
+        lists = guards.guarded((w.batch, w.num_kv_heads, self.sh.max_pages), torch.int32, dev,
+                               fill=-7, what="lists")
+        lens = guards.guarded((w.batch, w.num_kv_heads), torch.int32, dev, fill=-7, what="lens")
+        out = guards.guarded((w.batch, w.num_q_heads, w.head_dim), torch.float32, dev,
+                             fill=float("nan"), what="out")
+        lse = guards.guarded((w.batch, w.num_q_heads), torch.float32, dev, fill=float("nan"),
+                             what="lse")
         B.asp_coverage_select(kv, lay.q, gamma, budget, lists, lens, self.ws)
         B.asp_sparse_decode(kv, lay.q, lists, lens, 1.0 / math.sqrt(w.head_dim), out, lse, self.ws)
         assert B.asp_get_device_error(self.ws) == 0
@@ -205,6 +229,7 @@ def test_long128k_graph_sampled(cuda_device):
     case = Case(w, seed=0, device=cuda_device)
     q = torch.stack([lay.q for lay in case.layers])
     step = DecodeStep(case.kvs, q, gamma=0.99)
+    guard_outputs(step)
     step.capture()
     step.replay()
     torch.cuda.synchronize()
@@ -227,6 +252,7 @@ def test_graph_replay_matches_eager(cuda_device):
     case = Case(w, seed=6, device=cuda_device)
     q = torch.stack([lay.q for lay in case.layers])
     step = DecodeStep(case.kvs, q, gamma=0.97)
+    guard_outputs(step)
     step.run()
     torch.cuda.synchronize()
     eager = [t.clone() for t in (step.lists, step.lens, step.out, step.lse)]
@@ -279,10 +305,10 @@ def test_device_error_on_bad_page(cuda_device):
     w = small("bad", 2, 8, 2, 64, 16, 16 * 10)
     case = Case(w, seed=8, device=cuda_device)
     case.sh.block_table[1, 3] = case.sh.num_phys_pages + 1000
-    lists = torch.zeros((2, 2, case.sh.max_pages), dtype=torch.int32, device=cuda_device)
-    lens = torch.zeros((2, 2), dtype=torch.int32, device=cuda_device)
-    out = torch.zeros((2, 8, 64), device=cuda_device)
-    lse = torch.zeros((2, 8), device=cuda_device)
+    lists = guards.guarded((2, 2, case.sh.max_pages), torch.int32, cuda_device, fill=0)
+    lens = guards.guarded((2, 2), torch.int32, cuda_device, fill=0)
+    out = guards.guarded((2, 8, 64), torch.float32, cuda_device, fill=0)
+    lse = guards.guarded((2, 8), torch.float32, cuda_device, fill=0)
     B.asp_coverage_select(case.kvs[0], case.layers[0].q, 1.0, 0, lists, lens, case.ws)
     B.asp_sparse_decode(case.kvs[0], case.layers[0].q, lists, lens, 0.125, out, lse, case.ws)
     code = B.asp_get_device_error(case.ws)

@@ -21,7 +21,7 @@ import torch
 
 import oracle.asp_oracle as O
 from adaptive_sparse_paged_gb300 import binding as B
-from tests import parity
+from tests import guards, parity
 from tests.test_gpu_parity import SMALL, Case
 
 pytestmark = pytest.mark.gpu
@@ -33,8 +33,8 @@ REL = 4.6e-6
 def test_scores_match_oracle(cuda_device, w):
     case = Case(w, seed=3, device=cuda_device)
     kv, lay = case.kvs[0], case.layers[0]
-    scores = torch.full((w.batch, w.num_kv_heads, case.sh.max_pages), float("nan"),
-                        device=cuda_device)
+    scores = guards.guarded((w.batch, w.num_kv_heads, case.sh.max_pages), torch.float32,
+                            cuda_device, fill=float("nan"), what="scores")
     B.asp_page_scores(kv, lay.q, scores, case.ws)
     assert B.asp_get_device_error(case.ws) == 0
     sc = scores.cpu().numpy()

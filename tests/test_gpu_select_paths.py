@@ -26,7 +26,7 @@ import torch
 
 import oracle.asp_oracle as O
 from adaptive_sparse_paged_gb300 import binding as B
-from tests import parity
+from tests import guards, parity
 from tests.test_gpu_parity import Case, check_case, small
 
 pytestmark = pytest.mark.gpu
@@ -69,8 +69,9 @@ def test_clustered_scores(cuda_device, n_pages, gamma, budget):
     # the construction does what it says: one page far below, the rest packed
     spread = np.ptp(scores[1:])
     assert scores[0] < scores[1:].min() - 20.0 and spread < 24.0 / 4096
-    lists = torch.full((1, 1, case.sh.max_pages), -7, dtype=torch.int32, device=cuda_device)
-    lens = torch.full((1, 1), -7, dtype=torch.int32, device=cuda_device)
+    lists = guards.guarded((1, 1, case.sh.max_pages), torch.int32, cuda_device, fill=-7,
+                           what="lists")
+    lens = guards.guarded((1, 1), torch.int32, cuda_device, fill=-7, what="lens")
     B.asp_coverage_select(kv, case.layers[0].q, gamma, budget, lists, lens, case.ws)
     assert B.asp_get_device_error(case.ws) == 0
     k = int(lens[0, 0])

@@ -17,6 +17,7 @@ import torch
 
 from adaptive_sparse_paged_gb300 import binding as B
 from adaptive_sparse_paged_gb300 import synth
+from tests import guards
 
 pytestmark = pytest.mark.gpu
 
@@ -25,10 +26,12 @@ def _case(dev, seed):
     w = synth.Workload("noalloc", 3, 2, 16, 4, 128, 16, seq_len=1)
     sh = synth.make_shared(w, seed, dev, seq_lens=[16 * 300 + 7, 16 * 41, 5], max_pages=320)
     layers = [synth.make_layer(w, sh, seed, l, dev) for l in range(2)]
-    kvs = [B.PagedKV(lay.k_cache, lay.v_cache, B.new_summaries(lay.k_cache, sh.block_table),
+    summ_shape = (w.batch, w.num_kv_heads, sh.max_pages, 2, w.head_dim)
+    kvs = [B.PagedKV(lay.k_cache, lay.v_cache,
+                     guards.guarded(summ_shape, torch.bfloat16, dev, fill=0, what="summaries"),
                      sh.block_table, sh.seq_lens,
                      w.num_q_heads) for lay in layers]
-    ws = B.new_workspace(kvs[0])
+    ws = guards.guarded_workspace(kvs[0])
     for kv in kvs:
         B.asp_page_summarize(kv, B.ASP_SUMMARIZE_BULK, None, None, ws)
     assert B.asp_get_device_error(ws) == 0
@@ -50,8 +53,8 @@ def test_noalloc_matches_workspace_path_twice(cuda_device):
     err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
     got = []
     for kv, q, gamma, budget in calls:  # the no-allocation entry point, back to back
-        lists = torch.full(shape_l, -1, dtype=torch.int32, device=cuda_device)
-        lens = torch.full(shape_l[:2], -1, dtype=torch.int32, device=cuda_device)
+        lists = guards.guarded(shape_l, torch.int32, cuda_device, fill=-1, what="lists")
+        lens = guards.guarded(shape_l[:2], torch.int32, cuda_device, fill=-1, what="lens")
         B.asp_coverage_select_noalloc(kv, q, gamma, budget, lists, lens, err)
         got.append((lists, lens))
     torch.cuda.synchronize()
