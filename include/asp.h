@@ -37,6 +37,9 @@
  *   ASP_EUNSUPPORTED.
  * - The current CUDA device when a call is made must be the device that owns
  *   the pointers.
+ * - Tracing: every call opens an NVTX range named after itself (e.g.
+ *   "asp_sparse_decode"), so a profiler that reads NVTX attributes each
+ *   kernel to the call that launched it.
  */
 #ifndef ASP_H_
 #define ASP_H_
