@@ -64,6 +64,7 @@ struct ScoreParams {
   const int32_t* bt;
   int num_phys;
   int pf_pieces;  // pieces per warp fetched into L2 before the predecessor ends
+  uint32_t* fresh;  // set once scores are written to the workspace (or null)
 };
 
 // Three bf16 terms whose sum is x to fp32 precision: s0 = rn(x),
@@ -198,6 +199,7 @@ __global__ void __launch_bounds__(kScoreThreads, ScoreCfg<D, G>::kCtas)
     }
   }
   pdl_wait_predecessor();
+  if (p.fresh && blockIdx.x == 0 && threadIdx.x == 0) *p.fresh = 1u;
   // prefix of the requests' page counts N_b (clamped sequence lengths)
   if (warp == 0) {
     int carry = 0;
@@ -1149,7 +1151,7 @@ cudaError_t launch_score_tt(const SelectArgs& a, cudaStream_t stream) {
   ScoreParams p{kv.summaries, a.q, kv.seq_lens, a.scores, a.err, kv.batch, kv.num_q_heads,
                 kv.num_kv_heads, kv.page_size, kv.max_pages, 1.0f / sqrtf((float)D),
                 a.k_new, a.v_new, kv.k_cache, kv.v_cache, kv.block_table, kv.num_phys_pages,
-                kScorePrefetchPieces};
+                kScorePrefetchPieces, a.fresh};
   using C = ScoreCfg<D, G>;
   const size_t smem = (size_t)kScoreWarps * C::kSlots * (C::kSlotBytes + sizeof(uint64_t)) +
                       (3 * kv.batch + 2) * sizeof(int);
