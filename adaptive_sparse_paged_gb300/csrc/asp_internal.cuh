@@ -34,8 +34,9 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a bounded on-chip wait give
 // ----------------------------------------------------------------- workspace
 // [ header 256 B | merge_table int32[S] | scores f32[S*max_pages] | partials ]
 // header word 0 is the sticky device error mask; word 1 is set by the score
-// pass when it writes the scores region and cleared by the decode (a hint
-// for the decode's L2 prefetch, never read for a result).
+// pass when it writes the scores region and word 2 counts the selection's
+// finished segments; the decode clears both (hints for its L2 prefetch,
+// never read for a result).
 struct WsLayout {
   size_t table_off = 0;
   size_t scores_off = 0;
@@ -330,6 +331,7 @@ struct SelectArgs {
   const uint16_t* k_new = nullptr;
   const uint16_t* v_new = nullptr;
   uint32_t* fresh = nullptr;  // workspace word set once `scores` are written
+  uint32_t* done = nullptr;   // workspace word: segments whose selection is written
 };
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream);
 // The score kernel alone (a.scores: [B, Hkv, max_pages]; lists/lens unused).
@@ -350,6 +352,7 @@ struct DecodeArgs {
   int slot_floats;
   const float* scores = nullptr;  // the workspace's page scores (prefetch hint)
   uint32_t* fresh = nullptr;      // workspace word: scores written since the last decode
+  uint32_t* sel_done = nullptr;   // workspace word: segments the selection has finished
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 

@@ -433,6 +433,7 @@ struct SelectParams {
   int Hkv, P, max_pages;
   float gamma;
   int budget;
+  uint32_t* done;  // finished-segment count (or null)
 };
 
 // Order-preserving key: a larger score gives a larger key; -0 maps like +0.
@@ -511,7 +512,7 @@ __device__ __forceinline__ void block_minmax(float& mn, float& mx, float* scratc
 // known on the host), so the general path is compiled out and the kernel's
 // code, fetched afresh on every SM at each launch, is smaller.
 template <bool General>
-__global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
+__device__ __forceinline__ void select_segment(const SelectParams& p) {
   extern __shared__ __align__(16) uint8_t sel_smem[];
   uint32_t* hist = reinterpret_cast<uint32_t*>(sel_smem);  // [warp][bin][count, l0, l1, l2]
   float* cache = reinterpret_cast<float*>(hist + kSelWarps * kBins * 4);
@@ -1139,6 +1140,14 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
   if (tid == 0) p.lens[s] = (int32_t)(above_c + t);
 }
 
+template <bool General>
+__global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
+  select_segment<General>(p);
+  // This segment's result is written: count it out. The decode's L2
+  // prefetch runs only while this count is below the segment count.
+  if (p.done && threadIdx.x == 0) atomicAdd(p.done, 1u);
+}
+
 // Pieces per warp that the score pass fetches into L2 before the previous
 // kernel in the stream ends (the first three of its ring: 29 MB over the
 // grid at 128k and d = 128). Measured over a 32-layer step at 128k: none
@@ -1192,7 +1201,7 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
   SelectParams p{a.scores, kv.seq_lens, a.lists, a.lens, a.err, kv.num_kv_heads, kv.page_size,
-                 kv.max_pages, a.gamma, a.budget};
+                 kv.max_pages, a.gamma, a.budget, a.done};
   const bool general = kv.max_pages > kSelCache;
   const void* fn = general ? (const void*)select_kernel<true> : (const void*)select_kernel<false>;
   cudaError_t e = set_max_dynamic_smem(fn, (int)kSelSmem);
