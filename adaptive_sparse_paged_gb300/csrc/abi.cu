@@ -164,8 +164,7 @@ asp_status asp_coverage_select(const asp_paged_kv* kv, const float* q, float gam
   uint8_t* w = static_cast<uint8_t*>(ws);
   SelectArgs a{kv, q, gamma, budget, lists, lens, reinterpret_cast<float*>(w + lay.scores_off),
                reinterpret_cast<uint32_t*>(w), current_device_sm_count()};
-  a.fresh = reinterpret_cast<uint32_t*>(w) + 1;
-  a.done = reinterpret_cast<uint32_t*>(w) + 2;
+  a.fresh = a.done = reinterpret_cast<uint32_t*>(w) + 1;
   return from_cuda(launch_select(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -187,8 +186,7 @@ asp_status asp_coverage_select_append(const asp_paged_kv* kv, const uint16_t* k_
   uint8_t* w = static_cast<uint8_t*>(ws);
   SelectArgs a{kv, q, gamma, budget, lists, lens, reinterpret_cast<float*>(w + lay.scores_off),
                reinterpret_cast<uint32_t*>(w), current_device_sm_count(), k_new, v_new};
-  a.fresh = reinterpret_cast<uint32_t*>(w) + 1;
-  a.done = reinterpret_cast<uint32_t*>(w) + 2;
+  a.fresh = a.done = reinterpret_cast<uint32_t*>(w) + 1;
   return from_cuda(launch_select(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -224,7 +222,7 @@ asp_status asp_sparse_decode(const asp_paged_kv* kv, const float* q, const int32
                reinterpret_cast<int32_t*>(w + lay.table_off), reinterpret_cast<uint32_t*>(w),
                lay.decode_grid, lay.slot_floats,
                reinterpret_cast<const float*>(w + lay.scores_off),
-               reinterpret_cast<uint32_t*>(w) + 1, reinterpret_cast<uint32_t*>(w) + 2};
+               reinterpret_cast<uint32_t*>(w) + 1};
   return from_cuda(launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
 

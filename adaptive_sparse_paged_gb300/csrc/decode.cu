@@ -92,7 +92,6 @@ struct DecParams {
   // the caches, and the page-heads one CTA may prefetch
   const float* scores;
   uint32_t* fresh;
-  uint32_t* sel_done;
   const uint8_t* k_cache;
   const uint8_t* v_cache;
   int pf_cap;
@@ -171,8 +170,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   // that runs after its selection has finished, e.g. without programmatic
   // overlap, would only delay its own copies).
   if (p.fresh && p.pf_cap > 0 && cta < G - S) {
-    if (tid == 0)  // fresh scores, and the selection still running
-      flags[41] = __ldcg(p.fresh) != 0u && (!p.sel_done || __ldcg(p.sel_done) < (uint32_t)S);
+    if (tid == 0) {  // fresh scores, and the selection still running (one load)
+      const uint32_t v = __ldcg(p.fresh);
+      flags[41] = (v >> 31) != 0u && (v & 0x7fffffffu) < (uint32_t)S;
+    }
     __syncthreads();
     if (flags[41] != 0) {
       const int s = cta % S, part = cta / S;
@@ -211,10 +212,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     __syncthreads();  // flags[16..] and flags[40..41] are rewritten below
   }
   pdl_wait_predecessor();
-  if (p.fresh && cta == 0 && tid == 0) {  // the next hint needs a new selection
-    *p.fresh = 0u;
-    if (p.sel_done) *p.sel_done = 0u;
-  }
+  if (p.fresh && cta == 0 && tid == 0) *p.fresh = 0u;  // the next hint needs a new selection
   // ---- self-plan: lengths (validated) -> inclusive prefix in shared memory
   const int per = ceil_div(S, kDecThreads);
   const int a0 = min(S, tid * per), a1 = min(S, a0 + per);
@@ -691,7 +689,7 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
   DecParams p{a.q, a.lists, a.lens, kv.block_table, kv.seq_lens, a.out, a.lse, a.partials,
               a.merge_table, a.err, kv.batch, kv.num_q_heads, kv.num_kv_heads,
               kv.num_q_heads / kv.num_kv_heads, kv.max_pages, kv.num_phys_pages, a.slot_floats,
-              a.sm_scale * 1.4426950408889634f, a.scores, a.fresh, a.sel_done,
+              a.sm_scale * 1.4426950408889634f, a.scores, a.fresh,
               reinterpret_cast<const uint8_t*>(kv.k_cache),
               reinterpret_cast<const uint8_t*>(kv.v_cache), pf_cap};
   e = launch_pdl(decode_kernel<D, P, Deep>, dim3(a.grid), dim3(kDecThreads), smem, stream, tk, tv, p);

@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kScoreThreads, ScoreCfg<D, G>::kCtas)
     }
   }
   pdl_wait_predecessor();
-  if (p.fresh && blockIdx.x == 0 && threadIdx.x == 0) *p.fresh = 1u;
+  if (p.fresh && blockIdx.x == 0 && threadIdx.x == 0) *p.fresh = 0x80000000u;  // none done yet
   // prefix of the requests' page counts N_b (clamped sequence lengths)
   if (warp == 0) {
     int carry = 0;
