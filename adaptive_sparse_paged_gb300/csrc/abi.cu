@@ -164,7 +164,6 @@ asp_status asp_coverage_select(const asp_paged_kv* kv, const float* q, float gam
   uint8_t* w = static_cast<uint8_t*>(ws);
   SelectArgs a{kv, q, gamma, budget, lists, lens, reinterpret_cast<float*>(w + lay.scores_off),
                reinterpret_cast<uint32_t*>(w), current_device_sm_count()};
-  a.fresh = a.done = reinterpret_cast<uint32_t*>(w) + 1;
   return from_cuda(launch_select(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -186,7 +185,6 @@ asp_status asp_coverage_select_append(const asp_paged_kv* kv, const uint16_t* k_
   uint8_t* w = static_cast<uint8_t*>(ws);
   SelectArgs a{kv, q, gamma, budget, lists, lens, reinterpret_cast<float*>(w + lay.scores_off),
                reinterpret_cast<uint32_t*>(w), current_device_sm_count(), k_new, v_new};
-  a.fresh = a.done = reinterpret_cast<uint32_t*>(w) + 1;
   return from_cuda(launch_select(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -220,9 +218,7 @@ asp_status asp_sparse_decode(const asp_paged_kv* kv, const float* q, const int32
   DecodeArgs a{kv, q, lists, lens, sm_scale, out, lse,
                reinterpret_cast<float*>(w + lay.partials_off),
                reinterpret_cast<int32_t*>(w + lay.table_off), reinterpret_cast<uint32_t*>(w),
-               lay.decode_grid, lay.slot_floats,
-               reinterpret_cast<const float*>(w + lay.scores_off),
-               reinterpret_cast<uint32_t*>(w) + 1};
+               lay.decode_grid, lay.slot_floats};
   return from_cuda(launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -33,10 +33,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a bounded on-chip wait give
 
 // ----------------------------------------------------------------- workspace
 // [ header 256 B | merge_table int32[S] | scores f32[S*max_pages] | partials ]
-// header word 0 is the sticky device error mask. Word 1 is a hint for the
-// decode's L2 prefetch, never read for a result: the score pass sets it to
-// 2^31 when it writes the scores region, each select CTA adds 1 when its
-// segment is done, and the decode clears it.
+// header word 0 is the sticky device error mask.
 struct WsLayout {
   size_t table_off = 0;
   size_t scores_off = 0;
@@ -330,8 +327,6 @@ struct SelectArgs {
   // optional fused append (asp_coverage_select_append): bf16 [B, Hkv, d]
   const uint16_t* k_new = nullptr;
   const uint16_t* v_new = nullptr;
-  uint32_t* fresh = nullptr;  // workspace word 1 (score pass: set to 2^31)
-  uint32_t* done = nullptr;   // workspace word 1 (select CTAs: add 1 when done)
 };
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream);
 // The score kernel alone (a.scores: [B, Hkv, max_pages]; lists/lens unused).
@@ -350,8 +345,6 @@ struct DecodeArgs {
   uint32_t* err;
   int grid;
   int slot_floats;
-  const float* scores = nullptr;  // the workspace's page scores (prefetch hint)
-  uint32_t* fresh = nullptr;      // workspace word 1: 2^31 | selections done (or null)
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 

@@ -15,11 +15,6 @@
 // another CTA: under full HBM load each such round trip costs 1.5-2 us, and
 // at a piece end it would stall that CTA's copy pipeline.
 //
-// Before that (and before waiting on the selection that writes the lists),
-// the CTAs placed on the SMs that the selection leaves free prefetch into L2
-// the K/V pages that score near their segment's top (a hint: no result
-// depends on it; see the kernel).
-//
 // Data path (per CTA: 8 warps, one CTA per SM): every warp runs its own
 // pipeline. Warp w takes stages w, w+8, ... of the CTA's slice (a stage is a
 // 16-token sub-tile of one page: K then V, [16 rows x 64 channels] 2-D TMA
@@ -45,7 +40,6 @@
 
 #include <cudaTypedefs.h>
 
-#include <algorithm>
 #include <climits>
 
 #include <mutex>
@@ -88,19 +82,7 @@ struct DecParams {
   uint32_t* err;
   int B, Hq, Hkv, g, max_pages, num_phys, slot_floats;
   float scale_log2;
-  // speculative L2 prefetch (hint only): workspace scores, their fresh flag,
-  // the caches, and the page-heads one CTA may prefetch
-  const float* scores;
-  uint32_t* fresh;
-  const uint8_t* k_cache;
-  const uint8_t* v_cache;
-  int pf_cap;
 };
-
-// Pages whose score is within this of their segment's top score (weight at
-// least e^-2 of the top page's) are prefetched as likely members of the list.
-// Windows of 2, 3 and 4 measured alike at 128k.
-constexpr float kPrefetchWindow = 2.0f;
 
 // ------------------------------------------------------------ mma helpers
 __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
@@ -155,64 +137,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     prefix[0] = 0;
   }
   pdl_launch_dependents();
-  // ---- speculative L2 prefetch, before the wait (a hint: no result reads it).
-  // The selection that writes this call's lists runs on S SMs, one CTA per
-  // segment, and leaves HBM idle for several microseconds; the first G - S
-  // CTAs of this grid are placed on the other SMs meanwhile and wait. When
-  // the workspace's page scores are fresh (the score pass of the preceding
-  // selection has written them), each such CTA reads its segment's scores,
-  // takes their maximum and asks L2 for the K and V pages of its share of the
-  // segment that score within kPrefetchWindow of it: most of them are on the
-  // list that the decode reads next. Scores, lengths and table entries are
-  // read through L2 (bypassing L1); a stale value only changes which lines
-  // are fetched. The last S CTAs start after the selection and skip this, and
-  // so does every CTA once all S segments' selections are written (a decode
-  // that runs after its selection has finished, e.g. without programmatic
-  // overlap, would only delay its own copies).
-  if (p.fresh && p.pf_cap > 0 && cta < G - S) {
-    if (tid == 0) {  // fresh scores, and the selection still running (one load)
-      const uint32_t v = __ldcg(p.fresh);
-      flags[41] = (v >> 31) != 0u && (v & 0x7fffffffu) < (uint32_t)S;
-    }
-    __syncthreads();
-    if (flags[41] != 0) {
-      const int s = cta % S, part = cta / S;
-      const int nparts = (G - S - s + S - 1) / S;  // CTAs c < G - S with c % S == s
-      const int b = s / p.Hkv, h = s % p.Hkv;
-      const long long cap = (long long)p.max_pages * P;
-      const long long T0 = __ldcg(p.seq_lens + b);
-      const int N = ceil_div((int)(T0 < 0 ? 0 : (T0 > cap ? cap : T0)), P);
-      const float* sc = p.scores + (size_t)s * p.max_pages;
-      float mx = -INFINITY;
-      for (int i = tid; i < N; i += kDecThreads) mx = fmaxf(mx, __ldcg(sc + i));
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-      float* red = reinterpret_cast<float*>(flags + 16);  // [kDecWarps]
-      if (lane == 0) red[warp] = mx;
-      if (tid == 0) flags[40] = 0;
-      __syncthreads();
-      mx = red[0];
-#pragma unroll
-      for (int w = 1; w < kDecWarps; ++w) mx = fmaxf(mx, red[w]);
-      const float thr = mx - kPrefetchWindow;
-      const int p0 = (int)((long long)N * part / nparts);
-      const int p1 = (int)((long long)N * (part + 1) / nparts);
-      constexpr size_t kPageHead = (size_t)P * D * 2;
-      for (int i = p0 + tid; i < p1; i += kDecThreads) {
-        if (__ldcg(sc + i) >= thr && atomicAdd(&flags[40], 1) < p.pf_cap) {
-          const int ph = __ldcg(p.bt + (size_t)b * p.max_pages + i);
-          if (ph >= 0 && ph < p.num_phys) {
-            const size_t off = ((size_t)ph * p.Hkv + h) * kPageHead;
-            prefetch_l2_bulk(p.k_cache + off, (uint32_t)kPageHead);
-            prefetch_l2_bulk(p.v_cache + off, (uint32_t)kPageHead);
-          }
-        }
-      }
-    }
-    __syncthreads();  // flags[16..] and flags[40..41] are rewritten below
-  }
   pdl_wait_predecessor();
-  if (p.fresh && cta == 0 && tid == 0) *p.fresh = 0u;  // the next hint needs a new selection
   // ---- self-plan: lengths (validated) -> inclusive prefix in shared memory
   const int per = ceil_div(S, kDecThreads);
   const int a0 = min(S, tid * per), a1 = min(S, a0 + per);
@@ -678,20 +603,10 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
   CUtensorMap tk, tv;
   if ((e = make_page_map(&tk, kv.k_cache, rows, D, P)) != cudaSuccess) return e;
   if ((e = make_page_map(&tv, kv.v_cache, rows, D, P)) != cudaSuccess) return e;
-  // prefetch budget: 96 MiB of K/V over the grid (three quarters of L2; the
-  // streamed pages carry evict-first). Measured over the 32-layer step at
-  // 128k, same GPU: none 349.9 steps/s, 24 MiB 360.1, 48 MiB 363.5, 96 MiB
-  // 365.0; on another GPU 64 MiB 363.4, 96 MiB 364.3, 128 MiB 365.2,
-  // 192 MiB 364.8.
-  const long long pf_bytes = 96ll << 20;
-  const int pf_cap = (int)std::min<long long>(
-      1 << 20, pf_bytes / ((long long)a.grid * 2 * P * D * 2));
   DecParams p{a.q, a.lists, a.lens, kv.block_table, kv.seq_lens, a.out, a.lse, a.partials,
               a.merge_table, a.err, kv.batch, kv.num_q_heads, kv.num_kv_heads,
               kv.num_q_heads / kv.num_kv_heads, kv.max_pages, kv.num_phys_pages, a.slot_floats,
-              a.sm_scale * 1.4426950408889634f, a.scores, a.fresh,
-              reinterpret_cast<const uint8_t*>(kv.k_cache),
-              reinterpret_cast<const uint8_t*>(kv.v_cache), pf_cap};
+              a.sm_scale * 1.4426950408889634f};
   e = launch_pdl(decode_kernel<D, P, Deep>, dim3(a.grid), dim3(kDecThreads), smem, stream, tk, tv, p);
   if (e != cudaSuccess) return e;
   MergeParams mp{a.partials, a.merge_table, a.out, a.lse, kv.num_q_heads, kv.num_kv_heads,

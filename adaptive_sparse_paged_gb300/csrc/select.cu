@@ -64,7 +64,6 @@ struct ScoreParams {
   const int32_t* bt;
   int num_phys;
   int pf_pieces;  // pieces per warp fetched into L2 before the predecessor ends
-  uint32_t* fresh;  // set once scores are written to the workspace (or null)
 };
 
 // Three bf16 terms whose sum is x to fp32 precision: s0 = rn(x),
@@ -199,7 +198,6 @@ __global__ void __launch_bounds__(kScoreThreads, ScoreCfg<D, G>::kCtas)
     }
   }
   pdl_wait_predecessor();
-  if (p.fresh && blockIdx.x == 0 && threadIdx.x == 0) *p.fresh = 0x80000000u;  // none done yet
   // prefix of the requests' page counts N_b (clamped sequence lengths)
   if (warp == 0) {
     int carry = 0;
@@ -433,7 +431,6 @@ struct SelectParams {
   int Hkv, P, max_pages;
   float gamma;
   int budget;
-  uint32_t* done;  // finished-segment count (or null)
 };
 
 // Order-preserving key: a larger score gives a larger key; -0 maps like +0.
@@ -512,7 +509,7 @@ __device__ __forceinline__ void block_minmax(float& mn, float& mx, float* scratc
 // known on the host), so the general path is compiled out and the kernel's
 // code, fetched afresh on every SM at each launch, is smaller.
 template <bool General>
-__device__ __forceinline__ void select_segment(const SelectParams& p) {
+__global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
   extern __shared__ __align__(16) uint8_t sel_smem[];
   uint32_t* hist = reinterpret_cast<uint32_t*>(sel_smem);  // [warp][bin][count, l0, l1, l2]
   float* cache = reinterpret_cast<float*>(hist + kSelWarps * kBins * 4);
@@ -1140,14 +1137,6 @@ __device__ __forceinline__ void select_segment(const SelectParams& p) {
   if (tid == 0) p.lens[s] = (int32_t)(above_c + t);
 }
 
-template <bool General>
-__global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
-  select_segment<General>(p);
-  // This segment's result is written: count it out. The decode's L2
-  // prefetch runs only while this count is below the segment count.
-  if (p.done && threadIdx.x == 0) atomicAdd(p.done, 1u);
-}
-
 // Pieces per warp that the score pass fetches into L2 before the previous
 // kernel in the stream ends (the first three of its ring: 29 MB over the
 // grid at 128k and d = 128). Measured over a 32-layer step at 128k: none
@@ -1160,7 +1149,7 @@ cudaError_t launch_score_tt(const SelectArgs& a, cudaStream_t stream) {
   ScoreParams p{kv.summaries, a.q, kv.seq_lens, a.scores, a.err, kv.batch, kv.num_q_heads,
                 kv.num_kv_heads, kv.page_size, kv.max_pages, 1.0f / sqrtf((float)D),
                 a.k_new, a.v_new, kv.k_cache, kv.v_cache, kv.block_table, kv.num_phys_pages,
-                kScorePrefetchPieces, a.fresh};
+                kScorePrefetchPieces};
   using C = ScoreCfg<D, G>;
   const size_t smem = (size_t)kScoreWarps * C::kSlots * (C::kSlotBytes + sizeof(uint64_t)) +
                       (3 * kv.batch + 2) * sizeof(int);
@@ -1201,7 +1190,7 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
   SelectParams p{a.scores, kv.seq_lens, a.lists, a.lens, a.err, kv.num_kv_heads, kv.page_size,
-                 kv.max_pages, a.gamma, a.budget, a.done};
+                 kv.max_pages, a.gamma, a.budget};
   const bool general = kv.max_pages > kSelCache;
   const void* fn = general ? (const void*)select_kernel<true> : (const void*)select_kernel<false>;
   cudaError_t e = set_max_dynamic_smem(fn, (int)kSelSmem);

@@ -228,10 +228,6 @@ asp_status asp_page_scores(const asp_paged_kv* kv, const float* q, float* scores
  * log-sum-exp. A segment with lens 0 gets out = 0, lse = -inf.
  * K/V are bf16; the products run on tensor cores with fp32 accumulation and
  * the probabilities are rounded to bf16 for the P.V product.
- * When this call directly follows asp_coverage_select(_append) on the same
- * workspace and stream, the CTAs that start while the selection still runs
- * prefetch into L2 the K/V pages whose scores are near their segment's top
- * (up to 96 MiB): a hint only, the result never depends on it.
  * lists, lens : as written by asp_coverage_select (any order within a list).
  * out : fp32 [B, Hq, d]; lse : fp32 [B, Hq] (natural log).
  */
