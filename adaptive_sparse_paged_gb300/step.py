@@ -17,6 +17,11 @@ import torch
 from . import binding as B
 
 
+def _check_shape(name, t, shape):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
 class DecodeStep:
     def __init__(self, kvs, q, gamma: float, budget: int = 0, sm_scale: float | None = None,
                  append=None):
@@ -26,10 +31,16 @@ class DecodeStep:
         APPEND before each layer's selection.
         """
         self.kvs = list(kvs)
+        if not self.kvs:
+            raise ValueError("kvs must hold at least one layer")
         kv0 = self.kvs[0]
         L = len(self.kvs)
         dev = kv0.device
-        assert q.shape == (L, kv0.batch, kv0.num_q_heads, kv0.head_dim)
+        _check_shape("q", q, (L, kv0.batch, kv0.num_q_heads, kv0.head_dim))
+        if append is not None:
+            shp = (L, kv0.batch, kv0.num_kv_heads, kv0.head_dim)
+            _check_shape("append[0]", append[0], shp)
+            _check_shape("append[1]", append[1], shp)
         self.q = q
         self.gamma, self.budget = float(gamma), int(budget)
         self.sm_scale = sm_scale if sm_scale is not None else 1.0 / math.sqrt(kv0.head_dim)
@@ -111,11 +122,14 @@ class DecodeLoop:
         """kvs: PagedKV per layer; seq_lens0: int32 [B] (T0); q: fp32 [n, L, B, Hq, d];
         k_new, v_new: bf16 [n, L, B, Hkv, d]. fused_append: append inside the score
         pass (asp_coverage_select_append) instead of a separate APPEND launch."""
+        if not kvs:
+            raise ValueError("kvs must hold at least one layer")
         kv0 = kvs[0]
         n, L = q.shape[0], len(kvs)
-        assert q.shape == (n, L, kv0.batch, kv0.num_q_heads, kv0.head_dim)
-        assert k_new.shape == (n, L, kv0.batch, kv0.num_kv_heads, kv0.head_dim)
-        assert v_new.shape == k_new.shape
+        _check_shape("q", q, (n, L, kv0.batch, kv0.num_q_heads, kv0.head_dim))
+        _check_shape("k_new", k_new, (n, L, kv0.batch, kv0.num_kv_heads, kv0.head_dim))
+        _check_shape("v_new", v_new, tuple(k_new.shape))
+        _check_shape("seq_lens0", seq_lens0, (kv0.batch,))
         dev = kv0.device
         self.n, self.L = n, L
         self.q, self.k_new, self.v_new = q, k_new, v_new

@@ -81,3 +81,29 @@ def test_workspace_pointer_checks(lib):
     assert lib.asp_workspace_init(FAKE, 16, None) == B.ASP_EWORKSPACE
     code = ctypes.c_uint32(0)
     assert lib.asp_get_device_error(None, ctypes.byref(code), None) == B.ASP_EINVAL
+
+
+def test_step_shape_checks():
+    """DecodeStep / DecodeLoop reject mis-shaped inputs before touching a device."""
+    import torch
+    from adaptive_sparse_paged_gb300.step import DecodeLoop, DecodeStep
+
+    class FakeKV:  # the fields the constructors read before any allocation
+        batch, num_q_heads, num_kv_heads, head_dim, max_pages = 2, 8, 2, 64, 4
+        device = torch.device("cpu")
+
+    kv = FakeKV()
+    with pytest.raises(ValueError, match="q must have shape"):
+        DecodeStep([kv], torch.zeros(1, 2, 8, 32), gamma=0.9)
+    with pytest.raises(ValueError, match="at least one layer"):
+        DecodeStep([], torch.zeros(1, 2, 8, 64), gamma=0.9)
+    with pytest.raises(ValueError, match="append"):
+        DecodeStep([kv], torch.zeros(1, 2, 8, 64), gamma=0.9,
+                   append=(torch.zeros(1, 2, 2, 63), torch.zeros(1, 2, 2, 64)))
+    q = torch.zeros(3, 1, 2, 8, 64)
+    kn = torch.zeros(3, 1, 2, 2, 64)
+    with pytest.raises(ValueError, match="v_new"):
+        DecodeLoop([kv], torch.zeros(2, dtype=torch.int32), q, kn, torch.zeros(3, 1, 2, 2, 32),
+                   gamma=0.9)
+    with pytest.raises(ValueError, match="seq_lens0"):
+        DecodeLoop([kv], torch.zeros(3, dtype=torch.int32), q, kn, kn, gamma=0.9)
