@@ -86,6 +86,44 @@ def _segment_pages_no_table(cache, block_table, b, kv_head, seq_len):
     return np.stack([cache[base + p, kv_head] for p in range(n)])
 
 
+def _gather_whole_last_page(pages, ids, seq_len):
+    """Takes all P rows of every listed page, the partial last one included."""
+    rows = [pages[int(p)] for p in ids]
+    return np.concatenate(rows, axis=0) if rows else np.zeros((0, pages.shape[2]))
+
+
+def _num_pages_floor(seq_len, page_size):
+    return int(seq_len) // page_size
+
+
+def _page_mass_over_max(scores):
+    return np.exp(scores - scores.max())
+
+
+def _decode_step_interleaved_gqa(k_cache, v_cache, block_table, seq_lens, q, num_kv_heads,
+                                 gamma, budget=0, scale=None, lists=None, lens=None):
+    """Query head h reads KV head h % Hkv instead of h // g."""
+    B, hq, d = q.shape
+    o = np.zeros((B, hq, d))
+    lse = np.zeros((B, hq))
+    for b in range(B):
+        T = int(seq_lens[b])
+        for h in range(num_kv_heads):
+            kp = O.segment_pages(k_cache, block_table, b, h, T)
+            vp = O.segment_pages(v_cache, block_table, b, h, T)
+            heads = list(range(h, hq, num_kv_heads))
+            r = O.decode_segment(q[b, heads], kp, vp, T, gamma, budget, scale)
+            o[b, heads] = r["o"]
+            lse[b, heads] = r["lse"]
+    return {"o": o, "lse": lse, "ids": [], "scores": []}
+
+
+def _append_at_seq_len(k_cache, v_cache, block_table, seq_lens_after, k_new, v_new):
+    """Writes the new token one slot too far (position seq_len instead of seq_len - 1)."""
+    return O.__dict__["_orig_append_token"](k_cache, v_cache, block_table,
+                                            np.asarray(seq_lens_after) + 1, k_new, v_new)
+
+
 PLANTED = [
     ("page_scores", _no_scale),
     ("page_scores", _lower_bound),
@@ -98,6 +136,11 @@ PLANTED = [
     ("attend", _attend_no_scale),
     ("attend", _attend_k_for_v),
     ("segment_pages", _segment_pages_no_table),
+    ("gather_tokens", _gather_whole_last_page),
+    ("num_pages", _num_pages_floor),
+    ("page_mass", _page_mass_over_max),
+    ("decode_step", _decode_step_interleaved_gqa),
+    ("append_token", _append_at_seq_len),
 ]
 
 
