@@ -293,7 +293,50 @@ def check_append(o, seed=10):
         assert np.array_equal(summ[(1, h)][0], k_new[1, h]) and np.array_equal(summ[(1, h)][1], k_new[1, h])
 
 
+def check_bf16_decode(o, seed=11):
+    """bf16 bit patterns -> values: IEEE-defined patterns, and torch's own
+    bf16 -> fp32 widening (independent of the oracle's bit shift) on random
+    non-NaN patterns."""
+    fixed = {0x0000: 0.0, 0x3F80: 1.0, 0xBF80: -1.0, 0x4000: 2.0, 0xC000: -2.0,
+             0x3F81: 1.0 + 2.0 ** -7, 0x4049: 3.140625, 0x0001: 2.0 ** -133,
+             0x0080: 2.0 ** -126, 0x7F7F: (2.0 - 2.0 ** -7) * 2.0 ** 127,
+             0x7F80: math.inf, 0xFF80: -math.inf}
+    bits = np.array(list(fixed), dtype=np.uint16)
+    got = o.bf16_bits_to_f64(bits)
+    assert np.array_equal(got, np.array(list(fixed.values()))), got
+    neg0 = o.bf16_bits_to_f64(np.array([0x8000], dtype=np.uint16))[0]
+    assert neg0 == 0.0 and math.copysign(1.0, neg0) < 0
+    assert np.isnan(o.bf16_bits_to_f64(np.array([0x7FC0], dtype=np.uint16))[0])
+    import torch
+    rng = np.random.default_rng(seed)
+    rb = rng.integers(0, 1 << 16, 4096).astype(np.uint16)
+    rb = rb[(rb & 0x7F80) != 0x7F80]  # finite patterns only
+    want = torch.from_numpy(rb.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    assert np.array_equal(o.bf16_bits_to_f64(rb), want)
+    assert np.array_equal(o.bf16_bits_to_f64(rb.view(np.int16)), want)  # signed input too
+
+
+def check_segment_external_ids(o, seed=12):
+    """decode_segment with a given list attends over exactly that list: every
+    page given equals gamma = 1, an empty list gives 0 and -inf."""
+    rng = np.random.default_rng(seed)
+    P, d, T = 4, 8, 4 * 6 + 3
+    kp = _bf16_values(rng, (7, P, d))
+    vp = _bf16_values(rng, (7, P, d))
+    kp[2] += 3.0  # one page far above the rest, so gamma = 0.5 keeps fewer pages
+    q = np.abs(rng.standard_normal((2, d)))
+    own = o.decode_segment(q, kp, vp, T, gamma=0.5)
+    assert len(own["ids"]) < 7
+    full = o.decode_segment(q, kp, vp, T, gamma=0.5, ids=np.arange(7))
+    dense = o.decode_segment(q, kp, vp, T, gamma=1.0)
+    assert np.array_equal(full["o"], dense["o"]) and np.array_equal(full["lse"], dense["lse"])
+    none = o.decode_segment(q, kp, vp, T, gamma=0.5, ids=np.zeros(0, dtype=np.int64))
+    assert np.all(none["o"] == 0) and np.all(np.isneginf(none["lse"]))
+
+
 ALL_CHECKS = [
+    check_bf16_decode,
+    check_segment_external_ids,
     check_golden,
     check_summaries_attain_and_bound,
     check_scores_upper_bound,

@@ -124,6 +124,17 @@ def _append_at_seq_len(k_cache, v_cache, block_table, seq_lens_after, k_new, v_n
                                             np.asarray(seq_lens_after) + 1, k_new, v_new)
 
 
+def _bf16_shift_15(bits):
+    b = np.asarray(bits).astype(np.uint16).astype(np.uint32) << 15
+    return b.view(np.float32).astype(np.float64)
+
+
+def _segment_ignores_ids(q_group, k_pages, v_pages, seq_len, gamma, budget=0, scale=None,
+                         ids=None):
+    return O.__dict__["_orig_decode_segment"](q_group, k_pages, v_pages, seq_len, gamma,
+                                              budget, scale, None)
+
+
 PLANTED = [
     ("page_scores", _no_scale),
     ("page_scores", _lower_bound),
@@ -141,6 +152,8 @@ PLANTED = [
     ("page_mass", _page_mass_over_max),
     ("decode_step", _decode_step_interleaved_gqa),
     ("append_token", _append_at_seq_len),
+    ("bf16_bits_to_f64", _bf16_shift_15),
+    ("decode_segment", _segment_ignores_ids),
 ]
 
 
