@@ -107,3 +107,35 @@ def test_step_shape_checks():
                    gamma=0.9)
     with pytest.raises(ValueError, match="seq_lens0"):
         DecodeLoop([kv], torch.zeros(3, dtype=torch.int32), q, kn, kn, gamma=0.9)
+
+
+@pytest.mark.parametrize("over", [
+    dict(batch=512, num_q_heads=8, num_kv_heads=8, max_pages=1 << 20),  # page space >= 2^31
+    dict(num_phys_pages=1 << 27, num_kv_heads=2, page_size=16),         # TMA rows >= 2^31
+])
+def test_int32_index_limits(lib, over):
+    s = kv(**over)
+    size = ctypes.c_size_t(0)
+    assert lib.asp_workspace_size(ctypes.byref(s), ctypes.byref(size)) == B.ASP_EUNSUPPORTED
+
+
+@pytest.mark.parametrize("scale", [float("nan"), float("inf"), -0.1])
+def test_bad_decode_scale(lib, scale):
+    s = kv()
+    assert lib.asp_sparse_decode(ctypes.byref(s), FAKE, FAKE, FAKE, scale, FAKE, FAKE, FAKE,
+                                 1 << 20, None) == B.ASP_EINVAL
+
+
+def test_misaligned_decode_query(lib):
+    s = kv()
+    assert lib.asp_sparse_decode(ctypes.byref(s), FAKE + 4, FAKE, FAKE, 0.1, FAKE, FAKE, FAKE,
+                                 1 << 20, None) == B.ASP_EINVAL
+
+
+def test_noalloc_capacity_checked_first(lib):
+    """Shapes beyond the fixed scratch are rejected before any device work."""
+    s = kv(batch=4, num_q_heads=8, num_kv_heads=8, max_pages=(1 << 20) // 32 + 1)
+    assert lib.asp_coverage_select_noalloc(ctypes.byref(s), FAKE, 0.9, 0, FAKE, FAKE, None,
+                                           None) == B.ASP_EUNSUPPORTED
+    assert lib.asp_coverage_select_noalloc(None, FAKE, 0.9, 0, FAKE, FAKE, None,
+                                           None) == B.ASP_EINVAL
