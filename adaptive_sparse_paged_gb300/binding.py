@@ -37,6 +37,7 @@ EXPORTED = (
     "asp_sparse_decode",
     "asp_get_device_error",
     "asp_coverage_select_noalloc",
+    "asp_selftest_wait_timeout",
 )
 
 
@@ -93,6 +94,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "asp_sparse_decode": ([kvp, vp, vp, vp, ctypes.c_float, vp, vp, vp, sz, vp], i32),
             "asp_get_device_error": ([vp, u32p, vp], i32),
             "asp_coverage_select_noalloc": ([kvp, vp, ctypes.c_float, i32, vp, vp, vp, vp], i32),
+            "asp_selftest_wait_timeout": ([vp, sz, vp], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -298,6 +300,17 @@ def asp_coverage_select_noalloc(kv: PagedKV, q: torch.Tensor, gamma: float, budg
             kv.ref, q.data_ptr(), ctypes.c_float(gamma), int(budget), lists.data_ptr(),
             lens.data_ptr(), err_ptr, _stream_ptr(kv.device, stream)),
             "asp_coverage_select_noalloc")
+
+
+def asp_selftest_wait_timeout(ws: torch.Tensor, stream=None) -> None:
+    """Failure-detection self-test: a bounded on-chip wait that runs out (~2 s)
+    and sets ASP_DEVERR_TIMEOUT in `ws`'s error word (read it with
+    asp_get_device_error)."""
+    _need(ws, "ws", torch.uint8, ws.device)
+    with torch.cuda.device(ws.device):
+        _check(load_library().asp_selftest_wait_timeout(ws.data_ptr(), ws.numel(),
+                                                        _stream_ptr(ws.device, stream)),
+               "asp_selftest_wait_timeout")
 
 
 def asp_get_device_error(ws: torch.Tensor, stream=None) -> int:

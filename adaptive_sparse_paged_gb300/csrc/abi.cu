@@ -49,6 +49,18 @@ asp_status check_ws(const asp_paged_kv* kv, void* ws, size_t ws_bytes, WsLayout*
 }
 
 asp_status from_cuda(cudaError_t e) { return e == cudaSuccess ? ASP_OK : ASP_ECUDA; }
+
+// One warp; thread 0 waits on a barrier that expects one arrival which never
+// comes, through the library's bounded wait, and reports the timeout.
+__global__ void selftest_wait_kernel(uint32_t* err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0)) report(err, ASP_DEVERR_TIMEOUT);
+}
 }  // namespace
 
 int current_device_sm_count() {
@@ -220,6 +232,14 @@ asp_status asp_sparse_decode(const asp_paged_kv* kv, const float* q, const int32
                reinterpret_cast<int32_t*>(w + lay.table_off), reinterpret_cast<uint32_t*>(w),
                lay.decode_grid, lay.slot_floats};
   return from_cuda(launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+asp_status asp_selftest_wait_timeout(void* ws, size_t ws_bytes, asp_stream stream) {
+  NvtxRange range("asp_selftest_wait_timeout");
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < 256) return ASP_EWORKSPACE;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint32_t*>(ws));
+  return from_cuda(cudaGetLastError());
 }
 
 asp_status asp_get_device_error(void* ws, uint32_t* code_out, asp_stream stream) {

@@ -268,6 +268,18 @@ asp_status asp_coverage_select_noalloc(const asp_paged_kv* kv, const float* q, f
  */
 asp_status asp_get_device_error(void* ws, uint32_t* code_out, asp_stream stream);
 
+/*
+ * Self-test of failure detection (the pages have no counterpart). Every
+ * on-chip wait in this library is bounded: after 2 s it gives up, sets
+ * ASP_DEVERR_TIMEOUT in the device error word and the kernel returns, so a
+ * stuck copy never hangs the GPU. This call launches one small kernel whose
+ * thread waits, through the same bounded wait, on a shared-memory barrier
+ * that nothing completes: about 2 s later it sets the bit and returns, with
+ * nothing in flight. Read the result with asp_get_device_error; the context
+ * stays usable. ws: an initialised workspace (256-byte aligned, >= 256 B).
+ */
+asp_status asp_selftest_wait_timeout(void* ws, size_t ws_bytes, asp_stream stream);
+
 #ifdef __cplusplus
 }
 #endif
