@@ -2,7 +2,10 @@
 """Decode-step benchmark: coverage-selected sparse attention over a paged KV cache.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl asp|reference]
-                    [--config long128k] [--gamma 0.99]
+                    [--config long128k] [--gamma 0.99] [--budget 0] [--seed 1]
+
+--budget K > 0 keeps the top K pages per segment (the fixed-budget mode)
+instead of the coverage rule at --gamma, in both arms.
 
 One step = every layer of the workload through asp_coverage_select (score +
 select kernels) and asp_sparse_decode, replayed from one CUDA graph, with all
@@ -46,6 +49,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["asp", "reference"], default="asp")
     ap.add_argument("--config", default="long128k")
     ap.add_argument("--gamma", type=float, default=0.99)
+    ap.add_argument("--budget", type=int, default=0,
+                    help="keep the top BUDGET pages per segment instead of the coverage rule")
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
@@ -165,10 +170,11 @@ class ClockSampler:
                                     if r[4].replace(".", "").isdigit()), default=None)}
 
 
-def workload_name(w, gamma) -> str:
+def workload_name(w, gamma, budget=0) -> str:
     """The workload both arms report in config.workload."""
+    rule = f"budget{budget}" if budget > 0 else f"gamma{gamma}"
     return (f"{w.name}: B{w.batch} L{w.layers} Hq{w.num_q_heads} Hkv{w.num_kv_heads} "
-            f"d{w.head_dim} P{w.page_size} T{w.seq_len or 'lognormal'} gamma{gamma}")
+            f"d{w.head_dim} P{w.page_size} T{w.seq_len or 'lognormal'} {rule}")
 
 
 # ------------------------------------------------------------- oracle sample
@@ -261,7 +267,7 @@ def run_asp(args):
     torch.cuda.synchronize()
     gen_s = time.perf_counter() - t_gen
 
-    step = DecodeStep(kvs, q_all, gamma=args.gamma)
+    step = DecodeStep(kvs, q_all, gamma=args.gamma, budget=args.budget)
     step.capture()
     stream = torch.cuda.current_stream()
 
@@ -399,8 +405,9 @@ def run_asp(args):
         for kv in kvs:  # summaries of the first T0 tokens
             B.asp_page_summarize(kv, B.ASP_SUMMARIZE_BULK, None, None, ws0)
         steps_in = synth.make_steps(w, [lay.q for lay in layers], n_ms, seed, dev)
+        # the append fused into the score pass
         loop = DecodeLoop(kvs, t0.clone(), steps_in.q, steps_in.k_new, steps_in.v_new,
-                          gamma=args.gamma)  # append fused into the score pass
+                          gamma=args.gamma, budget=args.budget)
         loop.capture()
         loop.replay()  # the first run: fresh steps
         torch.cuda.synchronize()
@@ -412,7 +419,7 @@ def run_asp(args):
         del loop
         # the same loop with the append as its own kernel, for comparison
         sep = DecodeLoop(kvs, t0.clone(), steps_in.q, steps_in.k_new, steps_in.v_new,
-                         gamma=args.gamma, fused_append=False)
+                         gamma=args.gamma, budget=args.budget, fused_append=False)
         sep.capture()
         t_sep = max_over_ranks(timed_graph(sep, Km, 3), dist, dev)
         del sep
@@ -435,7 +442,8 @@ def run_asp(args):
         seg_layer = w.batch * w.num_kv_heads
         tasks = []
         for l in range(nl):
-            tasks += oracle_sample_tasks(w, sh, layers[l], seg_layer, args.gamma, 0, args.seed)
+            tasks += oracle_sample_tasks(w, sh, layers[l], seg_layer, args.gamma, args.budget,
+                                         args.seed)
         time_oracle(pool, tasks[:min(len(tasks), cores)])  # warm the workers
         t_cpu = time_oracle(pool, tasks)
         segs_per_step = seg_layer * w.layers
@@ -464,9 +472,10 @@ def run_asp(args):
             "dtype": "bf16",
             "data": "synthetic",
             "config": {
-                "workload": workload_name(w, args.gamma),
+                "workload": workload_name(w, args.gamma, args.budget),
                 "step": "all layers replayed from one CUDA graph",
                 "gamma": args.gamma,
+                "budget": args.budget,
                 "l2": "inputs larger than L2 (K/V %.1f GiB, summaries %.2f GiB resident); no flush"
                       % (2 * sh.num_phys_pages * Hkv * P * d * 2 * L / 2**30,
                          Bt * Hkv * sh.max_pages * 4 * d * L / 2**30),
@@ -521,7 +530,7 @@ def run_reference(args):
     lay = synth.make_layer(w, sh, args.seed, 0, dev)
     nseg = args.oracle_segments or max(8, cores)
     segs_per_step = w.batch * w.num_kv_heads * w.layers
-    tasks = oracle_sample_tasks(w, sh, lay, nseg, args.gamma, 0, args.seed)
+    tasks = oracle_sample_tasks(w, sh, lay, nseg, args.gamma, args.budget, args.seed)
     del lay
     for _ in range(max(0, min(args.warmup, 1))):
         time_oracle(pool, tasks[:min(len(tasks), cores)])
@@ -535,7 +544,8 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": workload_name(w, args.gamma), "gamma": args.gamma,
+        "config": {"workload": workload_name(w, args.gamma, args.budget), "gamma": args.gamma,
+                   "budget": args.budget,
                    "step": "fp64 oracle on the host cores, bounded sample per step"},
         "cpu_baseline": {"value": value, "unit": "steps/s", "cores": cores, "kind": "oracle",
                          "sample": f"each step: {len(tasks)} of {segs_per_step} segments of "

@@ -49,3 +49,13 @@ def test_traffic_follows_the_profiled_source(tmp_path, monkeypatch):
         open(bench.os.path.join(bench.ROOT, "profiles", "decode_kernel_ncu.md")).read())
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.decode_traffic_per_page("long128k") is None
+
+
+def test_reference_line_budget_mode(capsys, monkeypatch):
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.delenv("RANK", raising=False)
+    bench.main(["--impl", "reference", "--config", "tiny", "--steps", "1", "--warmup", "0",
+                "--oracle-segments", "2", "--budget", "5"])
+    d = json.loads([l for l in capsys.readouterr().out.splitlines() if l.startswith("{")][0])
+    assert d["config"]["budget"] == 5 and d["config"]["workload"].endswith("budget5")
+    assert d["value"] > 0
