@@ -72,3 +72,20 @@ def test_bench_imports_the_oracle_only_inside_functions():
         if isinstance(node, (ast.Import, ast.ImportFrom)):
             mod = node.module if isinstance(node, ast.ImportFrom) else node.names[0].name
             assert not (mod or "").startswith("oracle")
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without libasp.so every call raises: there is no CPU fallback."""
+    code = ("import sys; sys.path.insert(0, %r)\n"
+            "import torch\n"
+            "from adaptive_sparse_paged_gb300 import binding as B\n"
+            "B.LIB_PATH = %r\n"
+            "try:\n"
+            "    B.load_library(B.LIB_PATH)\n"
+            "except RuntimeError as e:\n"
+            "    assert 'libasp.so not found' in str(e), e\n"
+            "else:\n"
+            "    raise SystemExit('loaded a library that does not exist')\n"
+            % (ROOT, str(tmp_path / "libasp.so")))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr + r.stdout
