@@ -27,3 +27,9 @@ def _guard_bands():
     from tests import guards
     if guards.registered():
         guards.check_guards()
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """Writes the list-verdict tallies when ASP_PARITY_REPORT names a file."""
+    if "tests.parity" in sys.modules:
+        sys.modules["tests.parity"].write_report()

@@ -60,7 +60,7 @@ def test_decode_loop_matches_oracle(cuda_device, gamma, budget):
     kn, vn = parity.bf16_np(steps.k_new), parity.bf16_np(steps.v_new)
     lists, lens = loop.lists.cpu().numpy(), loop.lens.cpu().numpy()
     out, lse = loop.out.cpu().numpy(), loop.lse.cpu().numpy()
-    verdicts = {"exact": 0, "accepted": 0}
+    tally = parity.VerdictCounts(f"multistep {w.name} gamma {gamma} budget {budget}")
     for l, (lay, kv) in enumerate(zip(case.layers, case.kvs)):
         k_all, v_all = parity.bf16_np(kv.k_cache), parity.bf16_np(kv.v_cache)
         summ = parity.bf16_np(kv.summaries)
@@ -87,14 +87,13 @@ def test_decode_loop_matches_oracle(cuda_device, gamma, budget):
                     k = int(lens[i, l, b, h])
                     ids = lists[i, l, b, h, :k]
                     v = parity.list_verdict(ids, ref["scores"], gamma, budget)
-                    assert v in verdicts, f"step {i} layer {l} segment {(b, h)}: {v}"
-                    verdicts[v] += 1
+                    tally.add(v, where=f"step {i} layer {l} segment {(b, h)}")
                     o_ref, lse_ref = O.attend(qg, O.gather_tokens(kpi, ids, T),
                                               O.gather_tokens(vpi, ids, T), scale)
                     parity.check_outputs(out[i, l, b, h * g:(h + 1) * g],
                                          lse[i, l, b, h * g:(h + 1) * g], o_ref, lse_ref,
                                          what=f"step {i} layer {l} segment {(b, h)}")
-    assert verdicts["exact"] > 0
+    assert tally.finish()["exact"] > 0
 
 
 def test_decode_loop_replay_is_stable(cuda_device):

@@ -78,6 +78,8 @@ def test_clustered_scores(cuda_device, n_pages, gamma, budget):
     ids = lists[0, 0, :k].cpu().numpy()
     assert np.all(np.diff(ids) > 0)
     verdict = parity.list_verdict(ids, scores, gamma, budget)
-    assert verdict in ("exact", "accepted"), verdict
+    tally = parity.VerdictCounts(f"clustered {n_pages} pages gamma {gamma} budget {budget}")
+    tally.add(verdict)
+    tally.finish()
     if budget == 0:  # thousands of pages share the cutoff bin
         assert k > 32
