@@ -21,8 +21,12 @@
 //
 // select_kernel  One CTA (1024 threads) per segment. Softmax weights
 //                exp(s - max) are turned into fixed point (2^37 = weight of
-//                the top page), so every sum is exact and order-independent
-//                and the result is deterministic. A first pass histograms
+//                the top page on segments of up to 8192 pages, 2^42 on
+//                longer ones), so every sum is exact and order-independent
+//                and the result is deterministic. Rounding each weight to
+//                the unit errs by at most half a unit per page, i.e. by at
+//                most N * 2^-38 (N <= 8192: 3.0e-8) or N * 2^-43 (N <= 2^20:
+//                1.2e-7) of the total mass. A first pass histograms
 //                the weights over 4096 bins linear in max - s; the bin where
 //                the running weight from the top reaches gamma times the
 //                total is one interval of score keys, usually a handful of
@@ -415,7 +419,7 @@ constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelCache = 8192;  // N up to this: the fast path (scores in registers and smem)
 constexpr int kPer = kSelCache / kSelThreads;  // elements per thread on the fast path
 constexpr int kBins = 256;
-constexpr int kLimbBits = 13;    // mass = l0 + l1 << 13 + l2 << 26, each limb < 2^13
+constexpr int kLimbBits = 14;    // mass = l0 + l1 << 14 + l2 << 28, each limb < 2^14
 constexpr int kWarpCand = 4096;  // candidates one warp finishes on (fits the histogram area)
 constexpr int kLinBins = 4096;   // bins of the first, linear round
 constexpr int kLinLoBits = 19;   // fast path: a weight is lo + hi << 19, both < 2^19
@@ -442,16 +446,22 @@ __device__ __forceinline__ uint32_t score_key(float s) {
 __device__ __forceinline__ float key_score(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
-// Softmax weight of a page relative to the top page, in 2^-37 units
-// (<= 2^37, so 8192 of them sum below 2^50 and the fast path's 19-bit limbs
-// sum below 2^32).
+// Softmax weight of a page relative to the top page, in units of 1/unit of
+// the top page's weight. The fast path (N <= 8192) uses unit = 2^37: 8192
+// weights sum below 2^50 and its 19-bit limbs below 2^32. Longer segments use
+// 2^42, so that rounding 2^20 weights moves their total by at most 2^-23 of
+// the top page; their sums (below 2^62) are 64-bit, and the radix rounds'
+// three 14-bit limbs hold 42 bits (per-warp limb sums stay below 2^32 up to
+// 2^18 elements per warp).
 // Rounded to the nearest integer (ties to even) by IEEE bit arithmetic on
 // the integer pipes, which have several times the throughput of the
 // conversion unit: below 2^22, adding 2^23 leaves the rounded integer in the
 // mantissa bits; from 2^23 on the float is an integer, its mantissa shifted
 // by the exponent; the band between takes one conversion instruction.
-__device__ __forceinline__ unsigned long long mass_fixed(float s, float smax) {
-  const float f = exp2f((s - smax) * 1.4426950408889634f) * 137438953472.0f;  // 2^37
+constexpr float kUnitFast = 137438953472.0f;       // 2^37
+constexpr float kUnitLong = 4398046511104.0f;      // 2^42
+__device__ __forceinline__ unsigned long long mass_fixed(float s, float smax, float unit) {
+  const float f = exp2f((s - smax) * 1.4426950408889634f) * unit;
   if (f < 4194304.0f) return __float_as_uint(f + 8388608.0f) & 0x7fffffu;
   if (f >= 8388608.0f) {
     const uint32_t u = __float_as_uint(f);
@@ -460,7 +470,7 @@ __device__ __forceinline__ unsigned long long mass_fixed(float s, float smax) {
   return __float2uint_rn(f);
 }
 
-// ceil(gamma * z) exactly, for 0 < gamma <= 1 and z < 2^52, in integers:
+// ceil(gamma * z) exactly, for 0 < gamma <= 1 and z < 2^64, in integers:
 // gamma = m * 2^-k with a 24-bit m, so gamma * z = (m * z) >> k rounded up
 // (the product needs up to 76 bits: high and low 64-bit words).
 __device__ __forceinline__ unsigned long long ceil_gamma_times(float gamma, unsigned long long z) {
@@ -569,7 +579,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
   block_minmax(lo_s, hi_s, red_f);
   const float* sc = fast ? cache : gsc;
   const float smax = hi_s;
-  auto weight = [&](float x) -> unsigned long long { return mass_mode ? mass_fixed(x, smax) : 1ull; };
+  const float unit = fast ? kUnitFast : kUnitLong;
+  auto weight = [&](float x) -> unsigned long long {
+    return mass_mode ? mass_fixed(x, smax, unit) : 1ull;
+  };
 
   // selection weights: fixed-point softmax mass, or 1 in budget mode. The
   // target (gamma times the total mass) comes out of the first pass's bin scan.
@@ -589,11 +602,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
   constexpr uint32_t kLimbMask = (1u << kLimbBits) - 1u;
 
   // First pass: one histogram of bins linear in the distance from the top score,
-  // smax - s, over at most 28 units in mass mode (a page further down has
-  // zero fixed-point mass). The bin index never increases with the score, so
+  // smax - s, over at most 28 units in mass mode, 31 on the general path (a
+  // page further down has zero fixed-point mass). The bin index never increases with the score, so
   // the bin where the running weight from the top reaches the target holds
   // one interval of keys, usually a handful.
-  const float span = mass_mode ? fminf(hi_s - lo_s, 28.f) : hi_s - lo_s;
+  // (28 units: e^-28 * 2^37 < 0.5; 31 units: e^-31 * 2^42 < 0.5)
+  const float span = mass_mode ? fminf(hi_s - lo_s, fast ? 28.f : 31.f) : hi_s - lo_s;
   const float inv_w = span > 0.f ? (float)kLinBins / span : 0.f;
   auto lin_bin = [&](float x) { return min(kLinBins - 1, (int)((smax - x) * inv_w)); };
   int jbin;
@@ -786,7 +800,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
           uint32_t* h = my_hist + ((k - lo) >> shift) * 4;
           atomicAdd(h, 1u);
           if (mass_mode) {
-            const unsigned long long m = mass_fixed(x, smax);
+            const unsigned long long m = mass_fixed(x, smax, unit);
             atomicAdd(h + 1, (uint32_t)m & kLimbMask);
             atomicAdd(h + 2, (uint32_t)(m >> kLimbBits) & kLimbMask);
             atomicAdd(h + 3, (uint32_t)(m >> (2 * kLimbBits)));
@@ -840,7 +854,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
               uint32_t* h = hist + ((k - lo) >> shift) * 4;
               atomicAdd(h, 1u);
               if (mass_mode) {
-                const unsigned long long m = mass_fixed(x, smax);
+                const unsigned long long m = mass_fixed(x, smax, unit);
                 atomicAdd(h + 1, (uint32_t)m & kLimbMask);
                 atomicAdd(h + 2, (uint32_t)(m >> kLimbBits) & kLimbMask);
                 atomicAdd(h + 3, (uint32_t)(m >> (2 * kLimbBits)));
@@ -880,7 +894,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
     unsigned long long t;
     if (mass_mode) {
       // t = ceil(rem / w): a float estimate corrected exactly in integers
-      const unsigned long long w = mass_fixed(key_score(tau), smax);
+      const unsigned long long w = mass_fixed(key_score(tau), smax, unit);
       const unsigned long long rem = target - above_w;
       if (w) {
         const float est = ceilf((float)rem / (float)w);
@@ -904,7 +918,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectParams p) {
   // from 2^22 up exceed every n_eq (at most 2^20) and need no refinement;
   // below that the float estimate is within one of the exact value.
   auto tie_mass = [&](uint32_t tau, unsigned long long above_w) -> unsigned long long {
-    const unsigned long long w = mass_fixed(key_score(tau), smax);
+    const unsigned long long w = mass_fixed(key_score(tau), smax, unit);
     if (!w) return 1ull << 40;  // ties of zero mass: all of them
     const unsigned long long rem = target - above_w;
     const float est = ceilf((float)rem / (float)w);
