@@ -65,8 +65,12 @@ def captured_mass_topk(scores: torch.Tensor, num_pages: torch.Tensor, k: int) ->
 
 
 def budget_diagnostics(kvs, q_all, gammas=(0.95, 0.98, 0.99, 0.995, 0.999),
-                       ref_gamma: float = 0.99) -> dict:
-    """kvs: PagedKV per layer; q_all fp32 [L, B, Hq, d]. Returns a JSON-ready dict."""
+                       ref_gamma: float = 0.99, detail: bool = False) -> dict:
+    """kvs: PagedKV per layer; q_all fp32 [L, B, Hq, d]. Returns a JSON-ready dict.
+
+    detail=True adds the per-segment arrays behind the summaries under
+    "detail": "lens" {gamma: int [L, B, Hkv]} and "captured" (float64
+    [L, B, Hkv], the fixed budget's captured mass; NaN where N_b = 0)."""
     kv0 = kvs[0]
     L, dev = len(kvs), kv0.device
     ws = B.new_workspace(kv0)
@@ -76,11 +80,13 @@ def budget_diagnostics(kvs, q_all, gammas=(0.95, 0.98, 0.99, 0.995, 0.999),
                         device=dev)
     out = {"segments": int(L * kv0.batch * kv0.num_kv_heads), "by_gamma": {}}
     lens_ref = None
+    lens_all = {}
     for gm in sorted(set(list(gammas) + [ref_gamma])):
         lens = torch.empty((L, kv0.batch, kv0.num_kv_heads), dtype=torch.int32, device=dev)
         for l, kv in enumerate(kvs):
             B.asp_coverage_select(kv, q_all[l], gm, 0, lists, lens[l], ws)
         ln = lens.cpu().numpy()
+        lens_all[gm] = ln
         if gm == ref_gamma:
             lens_ref = ln
         if gm in gammas:
@@ -93,10 +99,12 @@ def budget_diagnostics(kvs, q_all, gammas=(0.95, 0.98, 0.99, 0.995, 0.999),
                          device=dev)
     n_dev = torch.as_tensor(n_pages, device=dev)
     caps = []
+    cap_full = np.full((L, kv0.batch, kv0.num_kv_heads), np.nan)
     for l, kv in enumerate(kvs):
         B.asp_page_scores(kv, q_all[l], scores, ws)
         cap = captured_mass_topk(scores, n_dev, k)
         caps.append(cap[n_dev > 0].flatten())
+        cap_full[l][n_pages > 0] = cap[n_dev > 0].cpu().numpy()
     assert B.asp_get_device_error(ws) == 0
     cap = torch.cat(caps).cpu().numpy()
     out["fixed_budget_equal_bytes"] = {
@@ -107,4 +115,6 @@ def budget_diagnostics(kvs, q_all, gammas=(0.95, 0.98, 0.99, 0.995, 0.999),
                           "p50": float(np.quantile(cap, 0.5))},
         "segments_below_ref_gamma": float((cap < ref_gamma).mean()),
     }
+    if detail:
+        out["detail"] = {"lens": lens_all, "captured": cap_full}
     return out
