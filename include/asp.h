@@ -252,8 +252,10 @@ asp_status asp_sparse_decode(const asp_paged_kv* kv, const float* q,
  * current); make that first call before any stream capture. All calls share
  * the array and it keeps the last call's contents; calls that overlap on the
  * GPU (other streams, other host threads) race on it, so serialise them.
- * dev_error: optional device word (may be NULL); device-detected range
- * problems are OR-ed into it as ASP_DEVERR_* bits; the caller clears it.
+ * dev_error: optional device word; device-detected range problems are OR-ed
+ * into it as ASP_DEVERR_* bits and the caller clears it. With NULL they go to
+ * a spare word inside the library's array that no call reads back: device
+ * error bits are then discarded.
  */
 #define ASP_NOALLOC_MAX_SCORES (1u << 20)
 asp_status asp_coverage_select_noalloc(const asp_paged_kv* kv, const float* q, float gamma,
