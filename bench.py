@@ -27,7 +27,6 @@ import json
 import math
 import multiprocessing as mp
 import os
-import re
 import subprocess
 import sys
 import time
@@ -101,21 +100,30 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+TRAFFIC_RECORD = os.path.join("profiles", "decode_kernel_traffic.json")
+
+
+def source_digest(*names) -> str:
+    """sha256[:16] over the named kernel sources (csrc/), in order."""
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "adaptive_sparse_paged_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def decode_traffic_per_page(cfg_name: str):
-    """ncu DRAM bytes per selected (page, head) of the decode kernel, if the
-    committed profile was taken on the current kernel source; else None."""
-    src = os.path.join(ROOT, "adaptive_sparse_paged_gb300", "csrc", "decode.cu")
-    path = os.path.join(ROOT, "profiles", "decode_kernel_ncu.md")
+    """ncu DRAM bytes per selected (page, head) of the decode kernel from the
+    committed profile record, if it was taken on the current kernel source
+    (the record names the sources it hashed); else None."""
     try:
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        text = open(path).read()
-    except OSError:
+        with open(os.path.join(ROOT, TRAFFIC_RECORD)) as f:
+            rec = json.load(f)
+        if source_digest(*rec["sources"]) != rec["sources_sha256_16"]:
+            return None
+        return float(rec["dram_bytes_per_selected_page_head"])
+    except (OSError, KeyError, ValueError, TypeError):
         return None
-    m_hash = re.search(r"decode\.cu sha256\[:16\]:\s*([0-9a-f]{16})", text)
-    m_val = re.search(r"dram bytes per selected page-head:\s*([0-9.]+)", text)
-    if not m_hash or not m_val or m_hash.group(1) != digest:
-        return None
-    return float(m_val.group(1))
 
 
 class ClockSampler:
@@ -177,6 +185,16 @@ def workload_name(w, gamma, budget=0) -> str:
             f"d{w.head_dim} P{w.page_size} T{w.seq_len or 'lognormal'} {rule}")
 
 
+def bench_config(w, sh, gamma, budget) -> dict:
+    """The config object, identical in both arms for the same arguments."""
+    P, d, Hkv, L = w.page_size, w.head_dim, w.num_kv_heads, w.layers
+    kv_gib = 2 * sh.num_phys_pages * Hkv * P * d * 2 * L / 2**30
+    summ_gib = w.batch * Hkv * sh.max_pages * 4 * d * L / 2**30
+    return {"workload": workload_name(w, gamma, budget), "gamma": gamma, "budget": budget,
+            "l2": "inputs larger than L2 (K/V %.1f GiB, summaries %.2f GiB resident); no flush"
+                  % (kv_gib, summ_gib)}
+
+
 # ------------------------------------------------------------- oracle sample
 def _oracle_worker(args):
     import numpy as np
@@ -185,7 +203,7 @@ def _oracle_worker(args):
     kp = O.bf16_bits_to_f64(kbits)
     vp = O.bf16_bits_to_f64(vbits)
     r = O.decode_segment(qg, kp, vp, T, gamma, budget, scale)
-    return int(len(r["ids"])), float(np.abs(r["o"]).sum())
+    return np.asarray(r["ids"], dtype=np.int32), float(np.abs(r["o"]).sum())
 
 
 def _pool_init():
@@ -221,15 +239,16 @@ def oracle_sample_tasks(w, sh, layer, nseg, gamma, budget, seed):
         idx = sh.block_table[b, :n].long()
         kb = layer.k_cache[idx, h].contiguous().view(torch.int16).cpu().numpy()
         vb = layer.v_cache[idx, h].contiguous().view(torch.int16).cpu().numpy()
-        tasks.append((q[b, h * g:(h + 1) * g], kb, vb, T, gamma, budget,
+        tasks.append((q[b, h * g:(h + 1) * g], kb, vb, T, float(np.float32(gamma)), budget,
                       1.0 / math.sqrt(w.head_dim)))
-    return tasks
+    return tasks, pick
 
 
 def time_oracle(pool, tasks):
+    """Seconds for the oracle over `tasks`, and its results."""
     t0 = time.perf_counter()
-    pool.map(_oracle_worker, tasks, chunksize=1)
-    return time.perf_counter() - t0
+    res = pool.map(_oracle_worker, tasks, chunksize=1)
+    return time.perf_counter() - t0, res
 
 
 # ------------------------------------------------------------------- asp arm
@@ -435,17 +454,19 @@ def run_asp(args):
                  "query_change": "per step: layer queries + 0.25 * N(0, 1)"}
         del steps_in
 
-    cpu = None
+    cpu = list_parity = None
     if pool is not None:
         # two whole layers (every segment of layers 0 and 1), scaled to all L layers
         nl = min(2, w.layers)
         seg_layer = w.batch * w.num_kv_heads
-        tasks = []
+        tasks, where = [], []
         for l in range(nl):
-            tasks += oracle_sample_tasks(w, sh, layers[l], seg_layer, args.gamma, args.budget,
-                                         args.seed)
+            tk, pick = oracle_sample_tasks(w, sh, layers[l], seg_layer, args.gamma, args.budget,
+                                           args.seed)
+            tasks += tk
+            where += [(l, b, h) for (b, h) in pick]
         time_oracle(pool, tasks[:min(len(tasks), cores)])  # warm the workers
-        t_cpu = time_oracle(pool, tasks)
+        t_cpu, res = time_oracle(pool, tasks)
         segs_per_step = seg_layer * w.layers
         step_s = t_cpu * segs_per_step / len(tasks)
         cpu = {"value": 1.0 / step_s, "unit": "steps/s", "cores": cores, "kind": "oracle",
@@ -454,6 +475,19 @@ def run_asp(args):
                          f"{cores} spawn workers x 1 thread, inputs pickled to the workers; "
                          f"{t_cpu:.1f} s, extrapolated x{w.layers / nl:g} to a full step"}
         pool.close()
+        # the step's page lists on the same segments against the oracle's (one
+        # more replay: the multi-step graph above appended tokens to the caches)
+        step.replay()
+        torch.cuda.synchronize()
+        lists_c = step.lists.cpu().numpy()
+        lens_c = step.lens.cpu().numpy()
+        same = 0
+        for (l, b, h), (ids, _) in zip(where, res):
+            k = int(lens_c[l, b, h])
+            same += int(np.array_equal(np.sort(lists_c[l, b, h, :k]), ids))
+        list_parity = {"segments": len(res), "identical_to_oracle": same,
+                       "different": len(res) - same,
+                       "sample": "the cpu_baseline segments, lists of the step's graph"}
 
     if rank == 0:
         steps_per_s = world * args.steps / t_max
@@ -471,17 +505,11 @@ def run_asp(args):
             "vs_baseline": None,
             "dtype": "bf16",
             "data": "synthetic",
-            "config": {
-                "workload": workload_name(w, args.gamma, args.budget),
-                "step": "all layers replayed from one CUDA graph",
-                "gamma": args.gamma,
-                "budget": args.budget,
-                "l2": "inputs larger than L2 (K/V %.1f GiB, summaries %.2f GiB resident); no flush"
-                      % (2 * sh.num_phys_pages * Hkv * P * d * 2 * L / 2**30,
-                         Bt * Hkv * sh.max_pages * 4 * d * L / 2**30),
-                "parallelism": f"replica per GPU x{world} (requests shard, no collective)",
-                "setup_s": round(gen_s, 1),
-            },
+            "config": bench_config(w, sh, args.gamma, args.budget),
+            "step": "all layers replayed from one CUDA graph",
+            "parallelism": f"replica per GPU x{world} (requests shard, no collective)",
+            "setup_s": round(gen_s, 1),
+            "layer_us": round(1e3 * ms / L, 2),
             "selected_kv_gbs": round(world * step_bytes * args.steps / t_max / 1e9, 1),
             "hbm_frac_of_measured": round(step_bytes / (ms / 1e3) / 1e9 / peak, 4),
             "hbm_frac_of_nominal_8tbs": round(step_bytes / (ms / 1e3) / 1e12 / 8.0, 4),
@@ -492,6 +520,7 @@ def run_asp(args):
             "top30_budget": at30,
             "multi_step": multi,
             "budget_diagnostics": diag,
+            "list_parity": list_parity,
             "kernels_ms": {"select_avg": round(sel_avg_s * 1e3, 4),
                            "decode_avg": round(dec_avg_s * 1e3, 4)},
             "roofline": {
@@ -502,6 +531,7 @@ def run_asp(args):
                 "peak_kind": peak_kind,
                 "unit": "GB/s",
                 "frac": round(dec_gbs / peak, 4),
+                "frac_of_nominal_8tbs": round(dec_gbs / 8000.0, 4),
                 "traffic": None if traffic is None else round(traffic),
                 "algorithmic_bytes_per_launch": round(dec_bytes_avg),
             },
@@ -530,23 +560,31 @@ def run_reference(args):
     lay = synth.make_layer(w, sh, args.seed, 0, dev)
     nseg = args.oracle_segments or max(8, cores)
     segs_per_step = w.batch * w.num_kv_heads * w.layers
-    tasks = oracle_sample_tasks(w, sh, lay, nseg, args.gamma, args.budget, args.seed)
+    tasks, _ = oracle_sample_tasks(w, sh, lay, nseg, args.gamma, args.budget, args.seed)
     del lay
     for _ in range(max(0, min(args.warmup, 1))):
         time_oracle(pool, tasks[:min(len(tasks), cores)])
     t = 0.0
     for _ in range(args.steps):
-        t += time_oracle(pool, tasks) * segs_per_step / len(tasks)
+        t += time_oracle(pool, tasks)[0]
     pool.close()
-    value = args.steps / t
+    # Each timed step is the oracle over a sample of one layer's segments:
+    # steps and ms_per_step describe that timed work; value, in the metric's
+    # full decode steps per second, scales it to every segment of every layer.
+    scale = segs_per_step / len(tasks)
+    value = args.steps / (t * scale)
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": workload_name(w, args.gamma, args.budget), "gamma": args.gamma,
-                   "budget": args.budget,
-                   "step": "fp64 oracle on the host cores, bounded sample per step"},
+        "config": bench_config(w, sh, args.gamma, args.budget),
+        "step": f"fp64 oracle on the host cores over {len(tasks)} of the {segs_per_step} "
+                f"segments of a full step",
+        "extrapolation": {"segments_timed_per_step": len(tasks),
+                          "segments_per_full_step": segs_per_step, "factor": scale,
+                          "ms_per_full_step": 1e3 * t * scale / args.steps,
+                          "value_is": "full steps per second = steps / (timed seconds x factor)"},
         "cpu_baseline": {"value": value, "unit": "steps/s", "cores": cores, "kind": "oracle",
                          "sample": f"each step: {len(tasks)} of {segs_per_step} segments of "
                                    f"layer 0 through the fp64 oracle, scaled to a full step"},

@@ -1,5 +1,5 @@
 """bench.py's JSON contract on the CPU: the reference arm's line, and the
-traffic figure it takes from the committed decode profile.
+traffic figure it takes from the committed decode profile record.
 
 The reference arm times the fp64 oracle on the host cores, so it runs here
 on the smallest workload; the GPU arm prints the same keys plus the
@@ -35,18 +35,27 @@ def test_reference_line(capsys, monkeypatch):
     assert "2 of" in cb["sample"]
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["h2d_bytes_per_step"] == 0
-    assert abs(d["ms_per_step"] - 1e3 / d["value"]) < 1e-6 * d["ms_per_step"]
+    ex = d["extrapolation"]
+    assert ex["segments_timed_per_step"] == 2 and ex["segments_per_full_step"] == 2
+    # steps x ms_per_step is the time the oracle actually ran; value scales it
+    full_ms = d["ms_per_step"] * ex["factor"]
+    assert abs(full_ms - 1e3 / d["value"]) < 1e-6 * full_ms
+    assert abs(ex["ms_per_full_step"] - full_ms) < 1e-6 * full_ms
+    assert set(d["config"]) == {"workload", "gamma", "budget", "l2"}
 
 
 def test_traffic_follows_the_profiled_source(tmp_path, monkeypatch):
-    """The committed figure is used only while decode.cu is the profiled source."""
-    assert bench.decode_traffic_per_page("long128k") is not None
+    """The committed figure is used only while the hashed sources are the profiled ones."""
+    rec_path = bench.os.path.join(bench.ROOT, bench.TRAFFIC_RECORD)
+    rec = json.load(open(rec_path))
+    assert rec["sources_sha256_16"] == bench.source_digest(*rec["sources"])
+    assert bench.decode_traffic_per_page("long128k") == rec["dram_bytes_per_selected_page_head"]
     fake = tmp_path / "adaptive_sparse_paged_gb300" / "csrc"
     fake.mkdir(parents=True)
-    (fake / "decode.cu").write_text("// another kernel\n")
+    for n in rec["sources"]:
+        (fake / n).write_text("// another kernel\n")
     (tmp_path / "profiles").mkdir()
-    (tmp_path / "profiles" / "decode_kernel_ncu.md").write_text(
-        open(bench.os.path.join(bench.ROOT, "profiles", "decode_kernel_ncu.md")).read())
+    (tmp_path / bench.TRAFFIC_RECORD).write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.decode_traffic_per_page("long128k") is None
 
