@@ -33,6 +33,7 @@ EXPORTED = (
     "asp_page_summarize",
     "asp_coverage_select",
     "asp_coverage_select_append",
+    "asp_select_plan",
     "asp_page_scores",
     "asp_sparse_decode",
     "asp_get_device_error",
@@ -89,6 +90,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "asp_page_summarize": ([kvp, i32, vp, vp, vp, sz, vp], i32),
             "asp_coverage_select": ([kvp, vp, ctypes.c_float, i32, vp, vp, vp, sz, vp], i32),
             "asp_page_scores": ([kvp, vp, vp, vp, sz, vp], i32),
+            "asp_select_plan": ([kvp, ctypes.c_float, i32, i32, ctypes.POINTER(i32),
+                                 ctypes.POINTER(i32)], i32),
             "asp_coverage_select_append": ([kvp, vp, vp, vp, ctypes.c_float, i32, vp, vp, vp,
                                             sz, vp], i32),
             "asp_sparse_decode": ([kvp, vp, vp, vp, ctypes.c_float, vp, vp, vp, sz, vp], i32),
@@ -247,6 +250,16 @@ def asp_coverage_select_append(kv: PagedKV, k_new: torch.Tensor, v_new: torch.Te
             kv.ref, k_new.data_ptr(), v_new.data_ptr(), q.data_ptr(), ctypes.c_float(gamma),
             int(budget), lists.data_ptr(), lens.data_ptr(), ws.data_ptr(), ws.numel(),
             _stream_ptr(kv.device, stream)), "asp_coverage_select_append")
+
+
+def asp_select_plan(kv: PagedKV, gamma: float, budget: int = 0, append: bool = False):
+    """(kernels one selection call launches, cluster CTAs per segment or 0)."""
+    k, c = ctypes.c_int32(0), ctypes.c_int32(0)
+    with torch.cuda.device(kv.device):
+        _check(load_library().asp_select_plan(kv.ref, ctypes.c_float(gamma), int(budget),
+                                              int(bool(append)), ctypes.byref(k),
+                                              ctypes.byref(c)), "asp_select_plan")
+    return int(k.value), int(c.value)
 
 
 def asp_page_scores(kv: PagedKV, q: torch.Tensor, scores: torch.Tensor, ws: torch.Tensor,

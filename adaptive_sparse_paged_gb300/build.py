@@ -20,7 +20,8 @@ ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG_DIR, "libasp.so")
-SOURCES = ["abi.cu", "summarize.cu", "select.cu", "decode.cu", "noalloc.cu"]
+SOURCES = ["abi.cu", "summarize.cu", "select.cu", "select_cluster.cu", "decode.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -44,8 +45,8 @@ def build(verbose: bool = False, force: bool = False) -> str:
     """Compile every kernel source and link libasp.so; returns its path."""
     nvcc = _nvcc()
     srcs = [os.path.join(CSRC, s) for s in SOURCES]
-    deps = srcs + [os.path.join(CSRC, "asp_internal.cuh"), os.path.join(INCLUDE, "asp.h"),
-                   os.path.abspath(__file__)]
+    deps = srcs + [os.path.join(CSRC, "asp_internal.cuh"), os.path.join(CSRC, "score_common.cuh"),
+                   os.path.join(INCLUDE, "asp.h"), os.path.abspath(__file__)]
     if not force and os.path.exists(LIB_PATH):
         built = os.path.getmtime(LIB_PATH)
         if all(os.path.getmtime(d) <= built for d in deps):

@@ -179,6 +179,23 @@ asp_status asp_coverage_select(const asp_paged_kv* kv, const float* q, float gam
   return from_cuda(launch_select(a, static_cast<cudaStream_t>(stream)));
 }
 
+asp_status asp_select_plan(const asp_paged_kv* kv, float gamma, int32_t budget, int32_t append,
+                           int32_t* kernels, int32_t* cluster_ctas) {
+  asp_status st = check_kv(kv);
+  if (st != ASP_OK) return st;
+  if (!kernels || !cluster_ctas) return ASP_EINVAL;
+  if (budget < 0) return ASP_EINVAL;
+  if (budget == 0 && !(gamma > 0.0f && gamma <= 1.0f)) return ASP_EINVAL;
+  const int sms = current_device_sm_count();
+  if (sms <= 0) return ASP_ECUDA;
+  const bool all = budget == 0 && gamma >= 1.0f;
+  int C = 0;
+  if (!all && !append) C = cluster_select_ctas(*kv, sms);
+  *cluster_ctas = C;
+  *kernels = C > 0 ? 1 : (all && !append ? 1 : 2);
+  return ASP_OK;
+}
+
 asp_status asp_coverage_select_append(const asp_paged_kv* kv, const uint16_t* k_new,
                                       const uint16_t* v_new, const float* q, float gamma,
                                       int32_t budget, int32_t* lists, int32_t* lens, void* ws,

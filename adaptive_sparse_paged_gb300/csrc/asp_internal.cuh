@@ -331,6 +331,13 @@ struct SelectArgs {
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream);
 // The score kernel alone (a.scores: [B, Hkv, max_pages]; lists/lens unused).
 cudaError_t launch_scores(const SelectArgs& a, cudaStream_t stream);
+// Scoring and selection in one cluster kernel (select_cluster.cu): the
+// cluster size C to use for this shape on the current device (0: the shape
+// takes the two-kernel path), and the launch. Segments of kClusterSelectMinPages
+// to 8192 pages qualify; a.scores is not used.
+constexpr int kClusterSelectMinPages = 64;
+int cluster_select_ctas(const asp_paged_kv& kv, int num_sms);
+cudaError_t launch_cluster_select(const SelectArgs& a, int C, cudaStream_t stream);
 
 struct DecodeArgs {
   const asp_paged_kv* kv;
@@ -347,6 +354,12 @@ struct DecodeArgs {
   int slot_floats;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// A 2-D bf16 tensor map over [rows, inner] (row stride inner * 2 bytes) with
+// boxes of [box_rows, box_inner] elements, the 128-byte swizzle and zero
+// fill out of bounds (decode.cu). box_inner * 2 must be 128.
+cudaError_t encode_bf16_2d_swizzled(CUtensorMap* map, const void* base, unsigned long long inner,
+                                    unsigned long long rows, unsigned box_inner, unsigned box_rows);
 
 // Per-device helpers (abi.cu).
 int current_device_sm_count();

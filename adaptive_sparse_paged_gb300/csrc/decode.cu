@@ -560,18 +560,28 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [rows = num_phys*Hkv*P, D] bf16 viewed as 2-D; box = [16 rows x 64 channels].
-cudaError_t make_page_map(CUtensorMap* map, const void* base, long long rows, int D, int P) {
+}  // namespace
+
+cudaError_t encode_bf16_2d_swizzled(CUtensorMap* map, const void* base, unsigned long long inner,
+                                    unsigned long long rows, unsigned box_inner, unsigned box_rows) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
-  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  cuuint32_t box[2] = {64, 16};
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+  cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+namespace {
+
+// [rows = num_phys*Hkv*P, D] bf16 viewed as 2-D; box = [16 rows x 64 channels].
+cudaError_t make_page_map(CUtensorMap* map, const void* base, long long rows, int D, int P) {
+  return encode_bf16_2d_swizzled(map, base, (unsigned long long)D, (unsigned long long)rows, 64,
+                                 16);
 }
 
 // Dynamic shared memory of decode_kernel: 1 KiB alignment slack, the ring,

@@ -39,7 +39,7 @@
 //                is compiled out of the variant launched when max_pages is
 //                at most 8192).
 
-#include "asp_internal.cuh"
+#include "score_common.cuh"
 
 #include <type_traits>
 
@@ -70,47 +70,19 @@ struct ScoreParams {
   int pf_pieces;  // pieces per warp fetched into L2 before the predecessor ends
 };
 
-// Three bf16 terms whose sum is x to fp32 precision: s0 = rn(x),
-// s1 = rn(x - s0), s2 = rn(x - s0 - s1). Each residual is exact in fp32, and
-// bf16 x bf16 products are exact in fp32, so the tensor-core dot products
-// below carry the full fp32 query.
-__device__ __forceinline__ void split3_bf16(float x, float (&s)[3]) {
-  s[0] = __bfloat162float(__float2bfloat16_rn(x));
-  const float r1 = x - s[0];
-  s[1] = __bfloat162float(__float2bfloat16_rn(r1));
-  s[2] = __bfloat162float(__float2bfloat16_rn(r1 - s[1]));
-}
-
 // Summaries are stored per segment (request b, KV head h) in logical page
 // order, so this pass is one sequential stream with no block-table lookups.
 // The concatenated page space of all segments (segment-major) is split evenly
 // over the warps of a persistent grid. Each warp walks its slice as pieces of
-// up to kPieceBytes of one segment's pages; lane p bulk-copies page p of a
-// piece into the warp's own ring of slots (one mbarrier per slot, so no warp
-// ever waits on another). Pages sit at a stride of 4d + 16 bytes in shared
-// memory, which keeps the ldmatrix rows of 8 consecutive pages on distinct
-// banks.
-//
-// The score of 8 pages is one row.col mma chain: A = the group's queries,
-// one row per (split term, head), K = 2d with q- against the min row and q+
-// against the max row; B = the 8 pages' summaries (N = pages). Rows past
-// 3 * G are zero. Row r's head is r % G, and since G divides 8 a lane's rows
-// all share head (lane / 4) % G: the lane sums its rows, a butterfly over the
-// lanes of the other split terms completes each head's sum, and one over the
-// heads takes the max.
-constexpr int kPieceBytes = 4096;
-
+// up to 4 KiB of one segment's pages; lane p bulk-copies page p of a piece
+// into the warp's own ring of slots (one mbarrier per slot, so no warp ever
+// waits on another). The scores of 8 pages at a time come from
+// score::GroupQuery (the group's queries against the pages' summaries on the
+// tensor cores).
 template <int D, int G>
-struct ScoreCfg {
-  static constexpr int kPageBytes = 4 * D;                      // min and max rows
-  static constexpr int kPiecePages = kPieceBytes / kPageBytes;  // 8 (d 128) or 16 (d 64)
-  static constexpr int kStride = kPageBytes + 16;               // padded page stride in smem
-  static constexpr int kSlotBytes = kPiecePages * kStride;
-  static constexpr int kKs = 2 * D / 16;                        // k-steps of one page
-  static constexpr int kBlocks = (3 * G + 7) / 8;               // 8-row A blocks holding data
-  static constexpr int kMt = (kBlocks + 1) / 2;                 // m16 tiles
-  static constexpr int kCtas = kBlocks > 2 ? 1 : 2;             // CTAs per SM (registers)
-  static constexpr int kSlots = kCtas == 2 ? 3 : 6;             // ring depth per warp
+struct ScoreCfg : score::Cfg<D, G> {
+  static constexpr int kCtas = score::Cfg<D, G>::kBlocks > 2 ? 1 : 2;  // CTAs per SM (registers)
+  static constexpr int kSlots = kCtas == 2 ? 3 : 6;                     // ring depth per warp
 };
 
 // Position in a warp's slice: segment (b, h), logical page lp, and the index
@@ -124,7 +96,7 @@ __global__ void __launch_bounds__(kScoreThreads, ScoreCfg<D, G>::kCtas)
     score_kernel(ScoreParams p) {
   using C = ScoreCfg<D, G>;
   constexpr int kPiecePages = C::kPiecePages, kPageBytes = C::kPageBytes, kStride = C::kStride;
-  constexpr int kSlots = C::kSlots, kKs = C::kKs, kBlocks = C::kBlocks, kMt = C::kMt;
+  constexpr int kSlots = C::kSlots;
   extern __shared__ __align__(128) uint8_t score_smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   constexpr int kRingBytes = kScoreWarps * kSlots * C::kSlotBytes;
@@ -306,35 +278,13 @@ __global__ void __launch_bounds__(kScoreThreads, ScoreCfg<D, G>::kCtas)
   };
   for (int k = 0; k < kSlots && ic.pos < wend; ++k) issue();
 
-  // A operand: block bi holds rows 8 bi + lane / 4; qa[bi][ks] = the two
-  // registers of that row at k-step ks (k = 16 ks + 2 (lane % 4) + {0, 1}
-  // and the same + 8).
   const int g = lane >> 2, t = lane & 3;
-  uint32_t qa[kBlocks][kKs][2];
-  auto load_q = [&](int b, int h) {
-    const float* qp = p.q + ((size_t)b * p.Hq + h * G + g % G) * D;
-#pragma unroll
-    for (int ks = 0; ks < kKs; ++ks)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int k = 16 * ks + 2 * t + 8 * e;  // k < D: q- with the min row, else q+ with max
-        const float2 x = *reinterpret_cast<const float2*>(qp + (k < D ? k : k - D));
-        float s0[3], s1[3];
-        split3_bf16(k < D ? fminf(x.x, 0.f) : fmaxf(x.x, 0.f), s0);
-        split3_bf16(k < D ? fminf(x.y, 0.f) : fmaxf(x.y, 0.f), s1);
-#pragma unroll
-        for (int bi = 0; bi < kBlocks; ++bi) {
-          const int r = 8 * bi + g, sp = r / G;  // split term of row r (>= 3: zero row)
-          const float lo = sp == 0 ? s0[0] : sp == 1 ? s0[1] : sp == 2 ? s0[2] : 0.f;
-          const float hi = sp == 0 ? s1[0] : sp == 1 ? s1[1] : sp == 2 ? s1[2] : 0.f;
-          qa[bi][ks][e] = pack_bf16(lo, hi);
-        }
-      }
-  };
+  score::GroupQuery<D, G> gq;
+  auto load_q = [&](int b, int h) { gq.load(p.q + ((size_t)b * p.Hq + h * G) * D, lane); };
   int qseg = cc.b * p.Hkv + cc.h, k = 0;
   load_q(cc.b, cc.h);  // the first piece's queries load while its copies fly
   bool aborted = false;
-  const uint32_t lane_row = (uint32_t)((lane & 7) * kStride + (lane >> 3) * 16);
+  const uint32_t lane_row = score::GroupQuery<D, G>::lane_row(lane);
 #pragma unroll 1
   for (; cc.pos < wend; ++k) {
     const int slot = k % kSlots;
@@ -353,48 +303,8 @@ __global__ void __launch_bounds__(kScoreThreads, ScoreCfg<D, G>::kCtas)
 #pragma unroll
     for (int nt = 0; nt < kPiecePages / 8; ++nt) {
       if (nt * 8 >= n) break;  // warp-uniform
-      float acc[kMt][2][4];    // [m tile][min half, max half][fragment]
-#pragma unroll
-      for (int mt = 0; mt < kMt; ++mt)
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) acc[mt][c][j] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < kKs; ks += 2) {
-        uint32_t bf[4];  // (b0, b1) of k-step ks, then of ks + 1
-        ldsm_x4(sb + nt * 8 * kStride + ks * 32, bf);
-        constexpr int kHalfKs = kKs / 2;
-#pragma unroll
-        for (int mt = 0; mt < kMt; ++mt) {
-          const bool up = 2 * mt + 1 < kBlocks;
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const uint32_t a[4] = {qa[2 * mt][ks + u][0], up ? qa[2 * mt + up][ks + u][0] : 0u,
-                                   qa[2 * mt][ks + u][1], up ? qa[2 * mt + up][ks + u][1] : 0u};
-            mma16816(acc[mt][ks >= kHalfKs], a, bf[2 * u], bf[2 * u + 1]);
-          }
-        }
-      }
-      // this lane's rows share head g % G: columns 2t and 2t + 1
-      float x0 = 0.f, x1 = 0.f;
-#pragma unroll
-      for (int mt = 0; mt < kMt; ++mt)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          x0 += acc[mt][c][0] + acc[mt][c][2];
-          x1 += acc[mt][c][1] + acc[mt][c][3];
-        }
-#pragma unroll
-      for (int m = 4 * G; m <= 16; m <<= 1) {  // the other split terms of the head
-        x0 += __shfl_xor_sync(kFull, x0, m);
-        x1 += __shfl_xor_sync(kFull, x1, m);
-      }
-#pragma unroll
-      for (int m = 4; m < 4 * G; m <<= 1) {  // max over the group's heads
-        x0 = fmaxf(x0, __shfl_xor_sync(kFull, x0, m));
-        x1 = fmaxf(x1, __shfl_xor_sync(kFull, x1, m));
-      }
+      float x0, x1;
+      gq.tile(sb + nt * 8 * kStride, x0, x1);
       const int pg = nt * 8 + 2 * t;
       if (g == 0) {
         if (pg < n) out[pg] = x0 * p.inv_sqrt_d;
@@ -437,60 +347,12 @@ struct SelectParams {
   int budget;
 };
 
-// Order-preserving key: a larger score gives a larger key; -0 maps like +0.
-__device__ __forceinline__ uint32_t score_key(float s) {
-  uint32_t f = __float_as_uint(s);
-  if (f == 0x80000000u) f = 0u;
-  return (f & 0x80000000u) ? ~f : (f | 0x80000000u);
-}
-__device__ __forceinline__ float key_score(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-// Softmax weight of a page relative to the top page, in units of 1/unit of
-// the top page's weight. The fast path (N <= 8192) uses unit = 2^37: 8192
-// weights sum below 2^50 and its 19-bit limbs below 2^32. Longer segments use
-// 2^42, so that rounding 2^20 weights moves their total by at most 2^-23 of
-// the top page; their sums (below 2^62) are 64-bit, and the radix rounds'
-// three 14-bit limbs hold 42 bits (per-warp limb sums stay below 2^32 up to
-// 2^18 elements per warp).
-// Rounded to the nearest integer (ties to even) by IEEE bit arithmetic on
-// the integer pipes, which have several times the throughput of the
-// conversion unit: below 2^22, adding 2^23 leaves the rounded integer in the
-// mantissa bits; from 2^23 on the float is an integer, its mantissa shifted
-// by the exponent; the band between takes one conversion instruction.
-constexpr float kUnitFast = 137438953472.0f;       // 2^37
-constexpr float kUnitLong = 4398046511104.0f;      // 2^42
-__device__ __forceinline__ unsigned long long mass_fixed(float s, float smax, float unit) {
-  const float f = exp2f((s - smax) * 1.4426950408889634f) * unit;
-  if (f < 4194304.0f) return __float_as_uint(f + 8388608.0f) & 0x7fffffu;
-  if (f >= 8388608.0f) {
-    const uint32_t u = __float_as_uint(f);
-    return (unsigned long long)((u & 0x7fffffu) | 0x800000u) << (((u >> 23) & 0xffu) - 150u);
-  }
-  return __float2uint_rn(f);
-}
-
-// ceil(gamma * z) exactly, for 0 < gamma <= 1 and z < 2^64, in integers:
-// gamma = m * 2^-k with a 24-bit m, so gamma * z = (m * z) >> k rounded up
-// (the product needs up to 76 bits: high and low 64-bit words).
-__device__ __forceinline__ unsigned long long ceil_gamma_times(float gamma, unsigned long long z) {
-  const uint32_t u = __float_as_uint(gamma);
-  const uint32_t e = (u >> 23) & 0xffu;  // gamma >= 2^-126 is normal for every gamma passed
-  const unsigned long long m = (u & 0x7fffffu) | 0x800000u;
-  const int k = 150 - (int)e;  // gamma = m * 2^-k, k >= 23 for gamma <= 1
-  const unsigned long long lo = m * z, hi = __umul64hi(m, z);
-  if (k >= 128) return (lo | hi) ? 1ull : 0ull;
-  unsigned long long q;  // (hi:lo) >> k
-  bool rem;
-  if (k >= 64) {
-    q = hi >> (k - 64);
-    rem = lo != 0 || (k > 64 && (hi & ((1ull << (k - 64)) - 1ull)) != 0);
-  } else {
-    q = (lo >> k) | (k ? hi << (64 - k) : 0ull);
-    rem = (lo & ((1ull << k) - 1ull)) != 0;
-  }
-  return q + (rem ? 1ull : 0ull);
-}
+using score::ceil_gamma_times;
+using score::key_score;
+using score::kUnitFast;
+using score::kUnitLong;
+using score::mass_fixed;
+using score::score_key;
 
 // Block min and max of one float pair in a single pass (scratch: 2 x warps).
 __device__ __forceinline__ void block_minmax(float& mn, float& mx, float* scratch) {
@@ -1199,6 +1061,10 @@ cudaError_t launch_scores(const SelectArgs& a, cudaStream_t stream) {
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream) {
   const asp_paged_kv& kv = *a.kv;
   const bool all = a.budget <= 0 && a.gamma >= 1.0f;
+  if (!all && !a.k_new) {  // one cluster per segment scores and selects it in one pass
+    const int C = cluster_select_ctas(kv, a.num_sms);
+    if (C > 0) return launch_cluster_select(a, C, stream);
+  }
   if (!all || a.k_new) {  // gamma >= 1 keeps every page: no scores needed (but the append)
     cudaError_t e = launch_scores(a, stream);
     if (e != cudaSuccess) return e;

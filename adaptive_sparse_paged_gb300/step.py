@@ -54,11 +54,12 @@ class DecodeStep:
         self.ws = B.new_workspace(kv0)
         self.graph = None
 
-    # kernel launches of one step, per layer: score + select (select alone at
-    # gamma = 1), decode + merge, and the append kernel when enabled
+    # kernel launches of one step, per layer: the selection's (one cluster
+    # kernel, or a score pass and a select kernel; select alone at gamma = 1),
+    # decode + merge, and the append kernel when enabled
     @property
     def launches_per_step(self) -> int:
-        per = 2 if (self.budget > 0 or self.gamma < 1.0) else 1
+        per, _ = B.asp_select_plan(self.kvs[0], self.gamma, self.budget)
         return len(self.kvs) * (per + 2 + (1 if self.append is not None else 0))
 
     def run_layer(self, l: int, stream=None, events=None):
@@ -151,8 +152,9 @@ class DecodeLoop:
 
     @property
     def launches(self) -> int:
-        """Kernel launches of the whole loop: [append,] score, select, decode, merge."""
-        per = 2 if (self.budget > 0 or self.gamma < 1.0 or self.fused_append) else 1
+        """Kernel launches of the whole loop: [append,] the selection's, decode, merge."""
+        per, _ = B.asp_select_plan(self.kvs[0][0], self.gamma, self.budget,
+                                   append=self.fused_append)
         return self.n * self.L * ((0 if self.fused_append else 1) + per + 2)
 
     def run(self, stream=None):

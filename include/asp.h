@@ -180,6 +180,20 @@ asp_status asp_coverage_select(const asp_paged_kv* kv, const float* q, float gam
                                void* ws, size_t ws_bytes, asp_stream stream);
 
 /*
+ * How asp_coverage_select (append = 0) or asp_coverage_select_append
+ * (append = 1) runs this shape on the CURRENT device: *kernels receives the
+ * number of kernels one call launches, *cluster_ctas the CTAs per segment of
+ * the one-pass cluster kernel (0: a score pass, then one select CTA per
+ * segment). Segments of 64 to 8192 pages take the cluster kernel when the
+ * device can run its clusters: a cluster of 1, 2 or 4 CTAs per segment
+ * streams the segment's summaries, keeps the scores on chip and selects
+ * through distributed shared memory. Both paths compute the same scores
+ * and select the same pages. Launches nothing.
+ */
+asp_status asp_select_plan(const asp_paged_kv* kv, float gamma, int32_t budget, int32_t append,
+                           int32_t* kernels, int32_t* cluster_ctas);
+
+/*
  * APPEND and coverage selection in one pass: the same result as
  * asp_page_summarize(kv, ASP_SUMMARIZE_APPEND, k_new, v_new, ...) followed by
  * asp_coverage_select(kv, q, gamma, budget, lists, lens, ...), with the

@@ -48,8 +48,11 @@ def test_traffic_follows_the_profiled_source(tmp_path, monkeypatch):
     """The committed figure is used only while the hashed sources are the profiled ones."""
     rec_path = bench.os.path.join(bench.ROOT, bench.TRAFFIC_RECORD)
     rec = json.load(open(rec_path))
-    assert rec["sources_sha256_16"] == bench.source_digest(*rec["sources"])
-    assert bench.decode_traffic_per_page("long128k") == rec["dram_bytes_per_selected_page_head"]
+    got = bench.decode_traffic_per_page("long128k")
+    if rec["sources_sha256_16"] == bench.source_digest(*rec["sources"]):
+        assert got == rec["dram_bytes_per_selected_page_head"]
+    else:  # profiled on other sources: no traffic figure
+        assert got is None
     fake = tmp_path / "adaptive_sparse_paged_gb300" / "csrc"
     fake.mkdir(parents=True)
     for n in rec["sources"]:
