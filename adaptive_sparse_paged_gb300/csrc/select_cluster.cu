@@ -481,6 +481,39 @@ __global__ void __launch_bounds__(kCsThreads, 1)
   auto wgt = [&](float xs) -> unsigned long long {
     return mass_mode ? score::mass_fixed(xs, smax, score::kUnitFast) : 1ull;
   };
+  // Ties kept: the fewest that reach the target (at least one), lowest ids
+  // first; `above_tau` is the weight (count) of every page above tau, below
+  // the target by the choice of tau. From the candidates above / at tau per
+  // CTA (gtc, eqc) it sets this CTA's output offset and its share of the
+  // ties, and CTA 0 writes the list length. Run by one thread.
+  auto finish = [&](uint32_t tau, unsigned long long above_tau, const uint32_t* gtc,
+                    const uint32_t* eqc) {
+    uint32_t n_eq = 0;
+#pragma unroll
+    for (int c = 0; c < C; ++c) n_eq += eqc[c];
+    unsigned long long t;
+    if (mass_mode) {
+      const unsigned long long wt = wgt(score::key_score(tau));
+      t = wt ? (target > above_tau ? score::ceil_div_count(target - above_tau, wt) : 1ull) : n_eq;
+    } else {
+      t = target > above_tau ? target - above_tau : 1ull;
+    }
+    if (t < 1) t = 1;
+    if (t > n_eq) t = n_eq;
+    uint32_t off = 0, eq_before = 0;
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+      const uint32_t keep_eq =
+          (uint32_t)min((unsigned long long)eqc[c], t > eq_before ? t - eq_before : 0ull);
+      if (c == rank) {
+        res_off = off;
+        res_eq = keep_eq;
+      }
+      off += ctl.above_c[c] + gtc[c] + keep_eq;
+      eq_before += eqc[c];
+    }
+    if (rank == 0) p.lens[s] = (int32_t)off;
+  };
   // weight (mass mode) or count (budget mode) of every page with a key above
   // the current candidate range
   unsigned long long above = mass_mode ? above_w : (unsigned long long)above_c;
@@ -488,7 +521,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
   if (nc <= 32) {
     if (warp == 0) {  // one candidate per lane
       const bool has = lane < (int)nc;
-      int r;
+      int r = 0;
       const float cv = has ? cand_s[slot_of(lane, r)] : 0.f;
       const uint32_t ck = score::score_key(cv);
       const unsigned long long cm = has ? wgt(cv) : 0ull;
@@ -505,14 +538,21 @@ __global__ void __launch_bounds__(kCsThreads, 1)
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) best = max(best, __shfl_xor_sync(kFull, best, o));
       const unsigned at = __ballot_sync(kFull, reach && ck == best);
-      if (lane == __ffs(at) - 1) {
+      const unsigned long long above_tau = __shfl_sync(kFull, above + gt_w, __ffs(at) - 1);
+      // candidates above and at tau, per CTA (their lanes' regions)
+      uint32_t gtc[kCsMaxC], eqc[kCsMaxC];
+#pragma unroll
+      for (int c = 0; c < C; ++c) {
+        gtc[c] = __popc(__ballot_sync(kFull, has && r == c && ck > best));
+        eqc[c] = __popc(__ballot_sync(kFull, has && r == c && ck == best));
+      }
+      if (lane == 0) {
         rx_pick[0] = best;
-        rx_pick_w = above + gt_w;  // everything above tau
+        finish(best, above_tau, gtc, eqc);
       }
     }
     __syncthreads();
     tau = rx_pick[0];
-    above = rx_pick_w;
   } else {
     // exact radix rounds over the candidate keys until one key is left
     uint32_t klo = 0xffffffffu, khi = 0u;
@@ -614,47 +654,27 @@ __global__ void __launch_bounds__(kCsThreads, 1)
       __syncthreads();  // rx_pick is rewritten by the next round
     }
     tau = klo;  // and `above` is everything above it
-  }
-  // candidates above tau and at tau, per CTA of the cluster (ids are contiguous per CTA)
-  if (tid < kCsMaxC) rank_cnt[tid][0] = rank_cnt[tid][1] = 0;
-  __syncthreads();
-  for (uint32_t j = tid; j < nc; j += kCsThreads) {
-    int r;
-    const uint32_t kk = score::score_key(cand_s[slot_of(j, r)]);
-    if (kk > tau) atomicAdd(&rank_cnt[r][0], 1u);
-    else if (kk == tau) atomicAdd(&rank_cnt[r][1], 1u);
-  }
-  __syncthreads();
-  if (tid == 0) {
-    uint32_t n_eq = 0;
-    for (int c = 0; c < C; ++c) n_eq += rank_cnt[c][1];
-    // ties kept: the fewest reaching the target (at least one), lowest ids
-    // first; `above` is the weight (count) of every page above tau, below
-    // the target by the choice of tau
-    unsigned long long t;
-    if (mass_mode) {
-      const unsigned long long wt = wgt(score::key_score(tau));
-      t = wt ? (target > above ? score::ceil_div_count(target - above, wt) : 1ull) : n_eq;
-    } else {
-      t = target > above ? target - above : 1ull;
+    // candidates above tau and at tau, per CTA of the cluster (ids are contiguous per CTA)
+    if (tid < kCsMaxC) rank_cnt[tid][0] = rank_cnt[tid][1] = 0;
+    __syncthreads();
+    for (uint32_t j = tid; j < nc; j += kCsThreads) {
+      int r;
+      const uint32_t kk = score::score_key(cand_s[slot_of(j, r)]);
+      if (kk > tau) atomicAdd(&rank_cnt[r][0], 1u);
+      else if (kk == tau) atomicAdd(&rank_cnt[r][1], 1u);
     }
-    if (t < 1) t = 1;
-    if (t > n_eq) t = n_eq;
-    uint32_t off = 0, eq_before = 0;
-    for (int c = 0; c < C; ++c) {
-      const uint32_t eq_c = rank_cnt[c][1];
-      const uint32_t keep_eq =
-          (uint32_t)min((unsigned long long)eq_c, t > eq_before ? t - eq_before : 0ull);
-      if (c == rank) {
-        res_off = off;
-        res_eq = keep_eq;
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t gtc[kCsMaxC], eqc[kCsMaxC];
+#pragma unroll
+      for (int c = 0; c < C; ++c) {
+        gtc[c] = rank_cnt[c][0];
+        eqc[c] = rank_cnt[c][1];
       }
-      off += ctl.above_c[c] + rank_cnt[c][0] + keep_eq;
-      eq_before += eq_c;
+      finish(tau, above, gtc, eqc);
     }
-    if (rank == 0) p.lens[s] = (int32_t)off;
+    __syncthreads();
   }
-  __syncthreads();
 
   // ------------------------------------- 7. kept ids, ascending, per CTA
   const uint32_t out_off = res_off, eq_keep = res_eq;
