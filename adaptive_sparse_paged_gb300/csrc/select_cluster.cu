@@ -878,8 +878,13 @@ int cluster_select_ctas(const asp_paged_kv& kv, int num_sms) {
   while (C * kCsPages < kv.max_pages) C *= 2;
   // spread each segment over more SMs while the grid would leave a quarter idle
   while (C < kCsMaxC && S * C * 4 < num_sms * 3) C *= 2;
+  // Every cluster pays the selection's latency (~8 us) once: only when all of
+  // them run in one wave does that beat the two-kernel path, whose score pass
+  // spreads every page over the whole GPU and whose select kernel runs a
+  // 1024-thread CTA per segment (at 128k one wave: 32 clusters of 4 CTAs;
+  // with 64 requests of up to 8192 pages, 512 clusters of 4 would take 14).
   const int n = kv.head_dim == 128 ? resident_g<128>(kv, C) : resident_g<64>(kv, C);
-  return n > 0 ? C : 0;
+  return n >= S ? C : 0;
 }
 
 cudaError_t launch_cluster_select(const SelectArgs& a, int C, cudaStream_t stream) {

@@ -126,8 +126,13 @@ class Layer:
     hot: dict = field(default_factory=dict)  # (b, kv_head) -> list of hot logical pages
 
 
-def make_layer(w: Workload, sh: Shared, seed: int, layer: int, device) -> Layer:
-    """Draws one layer's caches and queries (on `device`)."""
+def make_layer(w: Workload, sh: Shared, seed: int, layer: int, device,
+               unit_shift: bool = False) -> Layer:
+    """Draws one layer's caches and queries (on `device`).
+
+    unit_shift: move hot keys by shift * q_hat (the literal unit-norm reading
+    of the configs) instead of shift * sqrt(d) * q_hat; the draws are otherwise
+    the same."""
     B, Hq, Hkv, d, P = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size
     g_grp = Hq // Hkv
     gk = _gen(seed, 10, layer, device=device)
@@ -159,7 +164,7 @@ def make_layer(w: Workload, sh: Shared, seed: int, layer: int, device) -> Layer:
             qg = q[b, h * g_grp:(h + 1) * g_grp].mean(0)
             qhat = qg / qg.norm()
             phys = bt_cpu[b, pages].to(torch.long).to(device)
-            blk = k[phys, h].float() + (s * math.sqrt(d)) * qhat
+            blk = k[phys, h].float() + (s * (1.0 if unit_shift else math.sqrt(d))) * qhat
             k[phys, h] = blk.to(torch.bfloat16)
             hot[(b, h)] = sorted(int(x) for x in pages)
     return Layer(k, v, q, hot)

@@ -406,6 +406,35 @@ def run_asp(args):
                 "hbm_frac_of_measured": round(b_bytes / (tb / Kb) / 1e9 / peak, 4)}
         del bstep
 
+    # Sensitivity to the generator's reading: the pages read when hot keys
+    # move by shift * q_hat (unit norm, the configs' literal wording) instead
+    # of shift * sqrt(d) * q_hat, on the first two layers of the same draws.
+    literal = None
+    if not args.no_diagnostics:
+        nl = min(2, w.layers)
+        lit_kvs, lit_q = [], []
+        for l in range(nl):
+            lay = synth.make_layer(w, sh, seed, l, dev, unit_shift=True)
+            summ = B.new_summaries(lay.k_cache, sh.block_table)
+            kv = B.PagedKV(lay.k_cache, lay.v_cache, summ, sh.block_table, sh.seq_lens,
+                           w.num_q_heads)
+            B.asp_page_summarize(kv, B.ASP_SUMMARIZE_BULK, None, None, ws0)
+            lit_kvs.append(kv)
+            lit_q.append(lay.q)
+        lit_lens = torch.zeros((nl, w.batch, w.num_kv_heads), dtype=torch.int32, device=dev)
+        lit_lists = torch.zeros((w.batch, w.num_kv_heads, sh.max_pages), dtype=torch.int32,
+                                device=dev)
+        for l in range(nl):
+            B.asp_coverage_select(lit_kvs[l], lit_q[l], args.gamma, args.budget, lit_lists,
+                                  lit_lens[l], ws0)
+        assert B.asp_get_device_error(ws0) == 0
+        lit_pages = float(lit_lens.sum())
+        literal = {"shift": "shift * q_hat (unit norm)", "layers": nl,
+                   "pages_read_frac": round(lit_pages / (float(n_pages.sum()) * Hkv * nl), 4),
+                   "pages_read_frac_same_layers_sqrt_d_shift":
+                       round(float(lens[:nl].sum()) / (float(n_pages.sum()) * Hkv * nl), 4)}
+        del lit_kvs, lit_q, lit_lens, lit_lists
+
     # required page fractions per gamma, and a fixed budget of equal bytes
     diag = None
     if not args.no_diagnostics:
@@ -520,6 +549,7 @@ def run_asp(args):
             "top30_budget": at30,
             "multi_step": multi,
             "budget_diagnostics": diag,
+            "pages_read_literal_unit_shift": literal,
             "list_parity": list_parity,
             "kernels_ms": {"select_avg": round(sel_avg_s * 1e3, 4),
                            "decode_avg": round(dec_avg_s * 1e3, 4)},

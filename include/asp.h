@@ -185,7 +185,7 @@ asp_status asp_coverage_select(const asp_paged_kv* kv, const float* q, float gam
  * number of kernels one call launches, *cluster_ctas the CTAs per segment of
  * the one-pass cluster kernel (0: a score pass, then one select CTA per
  * segment). Segments of 64 to 8192 pages take the cluster kernel when the
- * device can run its clusters: a cluster of 1, 2 or 4 CTAs per segment
+ * device runs all of its clusters at once: a cluster of 1, 2 or 4 CTAs per segment
  * streams the segment's summaries, keeps the scores on chip and selects
  * through distributed shared memory. Both paths compute the same scores
  * and select the same pages. Launches nothing.

@@ -44,3 +44,30 @@ def test_layer_hot_pages_and_seeding():
         # hot keys sit >= 1 * sqrt(d) further along q_hat than noise
         assert proj[hot].min() > proj[~hot].max() if (~hot).any() else True
         assert proj[hot].min() > 0.9 * math.sqrt(w.head_dim)
+
+
+def test_unit_shift_moves_hot_keys_by_q_hat_only():
+    """unit_shift keeps every draw and moves hot keys by shift * q_hat instead of
+    shift * sqrt(d) * q_hat: cold pages are identical, hot pages differ."""
+    import math
+
+    import torch
+
+    from adaptive_sparse_paged_gb300 import synth
+    w = synth.Workload("u", 1, 1, 4, 1, 64, 16, seq_len=16 * 20, hot=("count", 3, 3),
+                       shift=(2.0, 2.0))
+    sh = synth.make_shared(w, 0, "cpu")
+    a = synth.make_layer(w, sh, 0, 0, "cpu")
+    b = synth.make_layer(w, sh, 0, 0, "cpu", unit_shift=True)
+    assert torch.equal(a.q, b.q) and torch.equal(a.v_cache, b.v_cache)
+    hot = a.hot[(0, 0)]
+    assert hot == b.hot[(0, 0)] and len(hot) == 3
+    phys = sh.block_table[0, :sh.num_pages[0]].long()
+    cold = [i for i in range(sh.num_pages[0]) if i not in hot]
+    assert torch.equal(a.k_cache[phys[cold], 0], b.k_cache[phys[cold], 0])
+    qh = a.q[0].mean(0)
+    qh = qh / qh.norm()
+    # the mean hot key moves along q_hat by about shift * sqrt(d) vs shift
+    da = (a.k_cache[phys[hot], 0].float().mean((0, 1)) @ qh).item()
+    db = (b.k_cache[phys[hot], 0].float().mean((0, 1)) @ qh).item()
+    assert abs(da - 2.0 * math.sqrt(64)) < 1.0 and abs(db - 2.0) < 1.0
