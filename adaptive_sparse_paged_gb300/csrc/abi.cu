@@ -190,7 +190,7 @@ asp_status asp_select_plan(const asp_paged_kv* kv, float gamma, int32_t budget, 
   if (sms <= 0) return ASP_ECUDA;
   const bool all = budget == 0 && gamma >= 1.0f;
   int C = 0;
-  if (!all && !append) C = cluster_select_ctas(*kv, sms);
+  if (!all) C = cluster_select_ctas(*kv, sms);
   *cluster_ctas = C;
   *kernels = C > 0 ? 1 : (all && !append ? 1 : 2);
   return ASP_OK;

@@ -1061,7 +1061,7 @@ cudaError_t launch_scores(const SelectArgs& a, cudaStream_t stream) {
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream) {
   const asp_paged_kv& kv = *a.kv;
   const bool all = a.budget <= 0 && a.gamma >= 1.0f;
-  if (!all && !a.k_new) {  // one cluster per segment scores and selects it in one pass
+  if (!all) {  // one cluster per segment scores (and appends) and selects it in one pass
     const int C = cluster_select_ctas(kv, a.num_sms);
     if (C > 0) return launch_cluster_select(a, C, stream);
   }

@@ -38,6 +38,7 @@
 #include <cooperative_groups.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "score_common.cuh"
 
@@ -61,7 +62,7 @@ constexpr int kLimb = 14;                       // radix rounds: 3 limbs of 14 b
 constexpr int kFine = 16;                       // histogram bins per coarse bin
 
 struct CsParams {
-  const uint16_t* summ;
+  uint16_t* summ;  // written only by the append variant
   const float* q;
   const int32_t* seq_lens;
   int32_t* lists;
@@ -75,10 +76,13 @@ struct CsParams {
   // K/V of kept pages fetched into L2 for the decode that follows: the first
   // kv_pf_pages kept pages (in id order) of each CTA's range
   const int32_t* bt;
-  const uint16_t* k_cache;
-  const uint16_t* v_cache;
+  uint16_t* k_cache;  // written only by the append variant
+  uint16_t* v_cache;
   int num_phys;
   int kv_pf_pages;
+  // append variant: the new token's K and V rows, bf16 [B, Hkv, d]
+  const uint16_t* k_new;
+  const uint16_t* v_new;
 };
 
 // Cluster exchange block, one per CTA. Every field a CTA reads after a
@@ -118,7 +122,7 @@ __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
-template <int D, int G, int C>
+template <int D, int G, int C, bool Append>
 __global__ void __launch_bounds__(kCsThreads, 1)
     cluster_select_kernel(const __grid_constant__ CUtensorMap tm_summ, const CsParams p) {
   using L = CsLayout<D, G>;
@@ -197,8 +201,39 @@ __global__ void __launch_bounds__(kCsThreads, 1)
   const int Mr = min(N, base + M) - base;         // pages of this CTA
   int32_t* out = p.lists + (size_t)s * p.max_pages;
   const bool mass_mode = p.budget <= 0;
+  // Append variant: before the piece holding the segment's last page is
+  // copied, its warp writes the new token's K and V rows into slot
+  // (T - 1) % P of that page and folds the key into the page's summary (a
+  // fresh page, slot 0, takes the key as both bounds), as the APPEND
+  // summarize does; the fence orders those writes before the copy reads.
+  using LV = typename std::conditional<D == 128, uint2, uint32_t>::type;  // d / 32 channels
+  constexpr int kLRow = 2 * D / (int)sizeof(LV);                          // lane units per row
+  auto append_token = [&]() {
+    const int lp = N - 1, slot = (T - 1) % p.P;
+    const int phys = __ldg(p.bt + (size_t)b * p.max_pages + lp);
+    if (phys < 0 || phys >= p.num_phys) {
+      if (lane == 0) report(p.err, ASP_DEVERR_PAGE_RANGE);
+      return;
+    }
+    const size_t unit = (size_t)b * p.Hkv + h;
+    const size_t row = ((size_t)phys * p.Hkv + h) * p.P + slot;
+    const LV kn = reinterpret_cast<const LV*>(p.k_new + unit * D)[lane];
+    const LV vn = reinterpret_cast<const LV*>(p.v_new + unit * D)[lane];
+    reinterpret_cast<LV*>(p.k_cache + row * D)[lane] = kn;
+    reinterpret_cast<LV*>(p.v_cache + row * D)[lane] = vn;
+    LV* sm = reinterpret_cast<LV*>(p.summ + (seg_page0 + lp) * 2 * D) + lane;
+    if (slot == 0) {
+      sm[0] = kn;
+      sm[kLRow] = kn;
+    } else {
+      sm[0] = vmin(sm[0], kn);
+      sm[kLRow] = vmax(sm[kLRow], kn);
+    }
+    fence_proxy_async_global();
+  };
   // cluster-uniform early exits: no remote access has happened yet
   if (N == 0 || (mass_mode && p.gamma >= 1.0f) || (!mass_mode && p.budget >= N)) {
+    if (Append && N > 0 && warp == 0 && base <= N - 1 && N - 1 < base + Mr) append_token();
     for (int i = tid; i < Mr; i += kCsThreads) out[base + i] = base + i;
     if (rank == 0 && tid == 0) p.lens[s] = N;
     if (C > 1) cluster_wait();
@@ -222,6 +257,10 @@ __global__ void __launch_bounds__(kCsThreads, 1)
     // and are not scored
     auto issue = [&]() {
       const int slot = issued % kCsSlots;
+      if (Append && issue_pg + min(kPiecePages, whi - issue_pg) == N) {  // warp-uniform
+        append_token();
+        __syncwarp();
+      }
       if (lane == 0) {
         mbar_arrive_expect_tx(&full[slot], kCsPieceBytes);
         const int row = (int)seg_page0 + issue_pg;
@@ -754,11 +793,11 @@ constexpr int kCsPrefetchPieces = 3;
 // decode faster.
 constexpr int kCsKvPrefetchPages = 32;
 
-template <int D, int G, int C>
+template <int D, int G, int C, bool Append>
 cudaError_t launch_cs(const SelectArgs& a, cudaStream_t stream) {
   const asp_paged_kv& kv = *a.kv;
   using L = CsLayout<D, G>;
-  const void* fn = (const void*)cluster_select_kernel<D, G, C>;
+  const void* fn = (const void*)cluster_select_kernel<D, G, C, Append>;
   cudaError_t e = set_max_dynamic_smem(fn, L::kBytes);
   if (e != cudaSuccess) return e;
   CUtensorMap tm;
@@ -770,7 +809,7 @@ cudaError_t launch_cs(const SelectArgs& a, cudaStream_t stream) {
   CsParams p{kv.summaries, a.q, kv.seq_lens, a.lists, a.lens, a.err, kv.num_q_heads,
              kv.num_kv_heads, kv.page_size, kv.max_pages, 1.0f / sqrtf((float)D), a.gamma,
              a.budget, kCsPrefetchPieces, kv.block_table, kv.k_cache, kv.v_cache,
-             kv.num_phys_pages, kCsKvPrefetchPages};
+             kv.num_phys_pages, kCsKvPrefetchPages, a.k_new, a.v_new};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kv.batch * kv.num_kv_heads * C);
   cfg.blockDim = dim3(kCsThreads);
@@ -785,14 +824,14 @@ cudaError_t launch_cs(const SelectArgs& a, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, cluster_select_kernel<D, G, C>, tm, p);
+  return cudaLaunchKernelEx(&cfg, cluster_select_kernel<D, G, C, Append>, tm, p);
 }
 
 // Clusters of C CTAs that the current device runs at once (0: none fit).
 template <int D, int G, int C>
 int active_clusters() {
   using L = CsLayout<D, G>;
-  const void* fn = (const void*)cluster_select_kernel<D, G, C>;
+  const void* fn = (const void*)cluster_select_kernel<D, G, C, false>;
   if (set_max_dynamic_smem(fn, L::kBytes) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C);
@@ -806,7 +845,7 @@ int active_clusters() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, cluster_select_kernel<D, G, C>, &cfg) != cudaSuccess)
+  if (cudaOccupancyMaxActiveClusters(&n, cluster_select_kernel<D, G, C, false>, &cfg) != cudaSuccess)
     return 0;
   return n;
 }
@@ -830,9 +869,9 @@ int resident_clusters() {
 template <int D, int G>
 cudaError_t launch_cs_c(const SelectArgs& a, int C, cudaStream_t stream) {
   switch (C) {
-    case 1: return launch_cs<D, G, 1>(a, stream);
-    case 2: return launch_cs<D, G, 2>(a, stream);
-    case 4: return launch_cs<D, G, 4>(a, stream);
+    case 1: return a.k_new ? launch_cs<D, G, 1, true>(a, stream) : launch_cs<D, G, 1, false>(a, stream);
+    case 2: return a.k_new ? launch_cs<D, G, 2, true>(a, stream) : launch_cs<D, G, 2, false>(a, stream);
+    case 4: return a.k_new ? launch_cs<D, G, 4, true>(a, stream) : launch_cs<D, G, 4, false>(a, stream);
   }
   return cudaErrorInvalidValue;
 }

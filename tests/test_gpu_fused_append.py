@@ -7,7 +7,8 @@ through the two separate calls and one through the fused call; K and V
 caches, summaries, lists and lengths must be identical (all integer or
 exactly rounded bf16 data), for appends into a partial page, into slot 0 of a
 fresh page, into a one-token request and with an empty request, in mass and
-budget mode and at gamma = 1 (scores skipped, append still done).
+budget mode (a budget of every page included) and at gamma = 1 (scores
+skipped, append still done), on both selection paths.
 """
 
 import pytest
@@ -40,8 +41,11 @@ def _pair(dev, w, lens_before, seed):
     (128, 16, 4, [16 * 31, 1, 16 * 5 + 3]),            # slot 0 of a fresh page; 1 -> 2 tokens
     (64, 32, 2, [32 * 9 + 31, 32 * 3, 77]),
     (128, 64, 8, [64 * 7 + 10, 64 * 2, 63]),
+    # 64 pages or more: the cluster kernel scores, appends and selects
+    (128, 16, 4, [16 * 300 + 7, 16 * 100, 0]),
+    (64, 16, 2, [16 * 2100 + 5, 16 * 70, 9]),
 ])
-@pytest.mark.parametrize("gamma,budget", [(0.9, 0), (0.5, 5), (1.0, 0)])
+@pytest.mark.parametrize("gamma,budget", [(0.9, 0), (0.5, 5), (1.0, 0), (0.5, 100_000)])
 def test_fused_append_equals_separate_calls(cuda_device, d, P, g, lens, gamma, budget):
     Hkv = 2
     w = small(f"fused_d{d}_p{P}", len(lens), g * Hkv, Hkv, d, P, 1)
