@@ -28,8 +28,9 @@ asp_status check_kv(const asp_paged_kv* kv) {
   if (!is_pow2_le8(kv->num_q_heads / kv->num_kv_heads)) return ASP_EUNSUPPORTED;
   if ((long long)kv->batch * kv->num_kv_heads > kMaxSegments) return ASP_EUNSUPPORTED;
   if (kv->max_pages > kMaxPages) return ASP_EUNSUPPORTED;
-  // page-space and TMA row coordinates are int32
-  if ((long long)kv->batch * kv->num_kv_heads * kv->max_pages >= (1LL << 31)) return ASP_EUNSUPPORTED;
+  // page-space (with the decode's split weights) and TMA row coordinates are int32
+  if ((long long)kv->batch * kv->num_kv_heads * (kv->max_pages + kMaxPieceCost) >= (1LL << 31))
+    return ASP_EUNSUPPORTED;
   if ((long long)kv->num_phys_pages * kv->num_kv_heads * kv->page_size >= (1LL << 31))
     return ASP_EUNSUPPORTED;
   // 16-byte alignment of the cache bases (bulk and tensor copies)

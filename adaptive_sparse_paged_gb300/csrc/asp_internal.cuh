@@ -28,6 +28,16 @@ struct NvtxRange {
 
 constexpr int kMaxSegments = 4096;     // batch * Hkv handled by one call
 constexpr int kMaxPages = 1 << 20;     // max_pages bound (int32 page-space arithmetic)
+// The decode splits its page sequence by weight: a list's first page weighs
+// 1 + decode_piece_cost(d, P) pages, the pages a CTA streams (~80 KiB of
+// K and V) in the time that ending a piece (its warps' merge) stalls it.
+constexpr int kDecodePieceBytes = 80 * 1024;
+constexpr int kMaxPieceCost = 32;
+inline int decode_piece_cost(int head_dim, int page_size) {
+  const int page_bytes = 4 * page_size * head_dim;  // K and V, bf16
+  const int c = (kDecodePieceBytes + page_bytes / 2) / page_bytes;
+  return c < kMaxPieceCost ? c : kMaxPieceCost;
+}
 constexpr int kMaxGroup = 8;           // query heads per KV head (padded mma width)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a bounded on-chip wait gives up after 2 s
 

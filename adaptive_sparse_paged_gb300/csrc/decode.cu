@@ -5,12 +5,15 @@
 //
 // Plan (every CTA, on the device): load lens[B*Hkv] into shared memory and
 // take their inclusive prefix; the concatenated lists form one sequence of
-// `total` pages, split evenly over the G CTAs (the first total % G take one
-// position more), so shares differ by at most one page whatever the length
-// mix. A CTA's range cuts at most two segments; each (segment, CTA) piece
-// produces one partial (m, l, o) in slot segment + CTA of the workspace,
-// which is unique because both indices grow along the sequence; a segment
-// held whole by one CTA is written out directly. A small second kernel merges the split segments by
+// `total` pages. Each (segment, CTA) piece ends in a CTA-wide merge of the
+// warps' states, which drains that CTA's copy pipeline for about as long as
+// streaming ~80 KiB takes, so the first page of every non-empty list weighs
+// 1 + piece_cost pages and the sequence is split evenly by weight over the G
+// CTAs: a CTA whose range starts more lists takes fewer pages, and the split
+// still depends on the list lengths alone. Each piece produces one partial
+// (m, l, o) in slot segment + CTA of the workspace, which is unique because
+// both indices grow along the sequence; a segment held whole by one CTA is
+// written out directly. A small second kernel merges the split segments by
 // log-sum-exp. The streaming kernel thus never fences, counts or waits on
 // another CTA: under full HBM load each such round trip costs 1.5-2 us, and
 // at a piece end it would stall that CTA's copy pipeline.
@@ -81,6 +84,7 @@ struct DecParams {
   int32_t* merge_table;
   uint32_t* err;
   int B, Hq, Hkv, g, max_pages, num_phys, slot_floats;
+  int piece_cost;  // extra weight of a list's first page in the split, in pages
   float scale_log2;
 };
 
@@ -127,6 +131,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   int* flags = reinterpret_cast<int*>(full + kDecWarps * C::kSlots);    // [0..2] merge, [8..] scan
   int* prefix = flags + 48;                                              // [S + 1]
 
+  // Split weight at the start of each segment, W(prefix[s]) = prefix[s] +
+  // piece_cost * (non-empty segments before s); [S + 1] ints in the ring,
+  // read only while planning, before the first copy lands there.
+  int* wstart = reinterpret_cast<int*>(ring);
+
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.B * p.Hkv;
   const int G = gridDim.x, cta = blockIdx.x;
@@ -135,14 +144,16 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     for (int i = 0; i < kDecWarps * C::kSlots; ++i) mbar_init(&full[i], 1);
     mbar_fence_init();
     prefix[0] = 0;
+    wstart[0] = 0;
   }
   pdl_launch_dependents();
   pdl_wait_predecessor();
-  // ---- self-plan: lengths (validated) -> inclusive prefix in shared memory
+  // ---- self-plan: lengths (validated) -> inclusive prefix of pages and of
+  // non-empty segments in shared memory
   const int per = ceil_div(S, kDecThreads);
   const int a0 = min(S, tid * per), a1 = min(S, a0 + per);
-  int run = 0;
-  for (int s = a0; s < a1; ++s) {
+  int run = 0, nzr = 0;
+  for (int s = a0; s < a1; ++s) {  // wstart[s + 1] first holds non-empty segments up to s
     const int b = s / p.Hkv;
     const int n_b = ceil_div(clamp_seq_len(p.seq_lens[b], p.max_pages, P, p.err), P);
     int n = p.lens[s];
@@ -151,29 +162,69 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       n = n < 0 ? 0 : n_b;
     }
     run += n;
+    nzr += n > 0 ? 1 : 0;
     prefix[s + 1] = run;
+    wstart[s + 1] = nzr;
   }
-  int x = run;
+  int x = run, y = nzr;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(kFull, x, o);
-    if (lane >= o) x += y;
+    const int xo = __shfl_up_sync(kFull, x, o), yo = __shfl_up_sync(kFull, y, o);
+    if (lane >= o) {
+      x += xo;
+      y += yo;
+    }
   }
-  if (lane == 31) flags[8 + warp] = x;
+  if (lane == 31) {
+    flags[8 + warp] = x;
+    flags[16 + warp] = y;
+  }
   __syncthreads();
-  int off = 0;
-  for (int w = 0; w < warp; ++w) off += flags[8 + w];
+  int off = 0, offn = 0, total = 0;
+  for (int w = 0; w < kDecWarps; ++w) {
+    if (w < warp) {
+      off += flags[8 + w];
+      offn += flags[16 + w];
+    }
+    total += flags[8 + w];  // < 2^31, checked on the host
+  }
   off += x - run;
-  for (int s = a0; s < a1; ++s) prefix[s + 1] += off;
+  offn += y - nzr;
+  // Every share of the weight must hold a page (X + 1 <= share size), so that
+  // the CTAs holding pieces of one segment are consecutive, as the merge
+  // kernel assumes: X is capped at total / G - 1.
+  const int X = max(0, min(p.piece_cost, total / G - 1));
+  for (int s = a0; s < a1; ++s) {
+    prefix[s + 1] += off;
+    wstart[s + 1] = prefix[s + 1] + X * (wstart[s + 1] + offn);
+  }
   __syncthreads();
 
-  const int total = prefix[S];  // < 2^31, checked on the host
-  const int geff = total < G ? total : G;
-  const EvenSplit split(total, geff > 0 ? geff : 1);
+  // Weighted split: page j of segment s weighs 1, plus X when j = prefix[s];
+  // W(j) = weight of the pages before j. CTA c takes the pages whose W lies
+  // in the c-th even share of the total weight (< 2^31: the host checks
+  // B * Hkv * (max_pages + 32)).
+  const int wtotal = wstart[S];
+  const int geff = wtotal < G ? wtotal : G;
+  const EvenSplit split(wtotal, geff > 0 ? geff : 1);
+  auto weight_at = [&](int s, int j) {  // W(j) for page j of segment s
+    return j == prefix[s] ? wstart[s] : j + (wstart[s] - prefix[s]) + X;
+  };
+  auto page_at = [&](int cut) {  // first page j with W(j) >= cut
+    if (cut >= wtotal) return total;
+    int lo = 0, hi = S - 1;  // largest s with wstart[s] <= cut: a non-empty segment
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (wstart[mid] <= cut) lo = mid; else hi = mid - 1;
+    }
+    const int j0 = prefix[lo];
+    if (cut <= wstart[lo]) return j0;
+    return min(max(cut - (wstart[lo] - j0) - X, j0 + 1), prefix[lo + 1]);
+  };
   long long beg = 0, end = 0;
   if (cta < geff) {
-    beg = split.begin(cta);
-    end = split.end(cta);
+    beg = page_at(split.begin(cta));
+    end = page_at(split.end(cta));
   }
   const float kLn2 = 0.69314718055994530942f;
 
@@ -191,12 +242,14 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     for (int s = tid; s < S; s += kDecThreads) {
       int t = 0;
       if (prefix[s + 1] > prefix[s]) {
-        const int cf = split.part_of(prefix[s]), cl = split.part_of(prefix[s + 1] - 1);
+        const int cf = split.part_of(wstart[s]);
+        const int cl = split.part_of(weight_at(s, prefix[s + 1] - 1));
         t = (cf << 16) | cl;
       }
       p.merge_table[s] = t;
     }
   }
+  __syncthreads();  // the weights are done with: the ring is free for copies
   if (beg >= end) return;
   if (tid == 0) {
     prefetch_tensormap(&tmK);
@@ -616,7 +669,7 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
   DecParams p{a.q, a.lists, a.lens, kv.block_table, kv.seq_lens, a.out, a.lse, a.partials,
               a.merge_table, a.err, kv.batch, kv.num_q_heads, kv.num_kv_heads,
               kv.num_q_heads / kv.num_kv_heads, kv.max_pages, kv.num_phys_pages, a.slot_floats,
-              a.sm_scale * 1.4426950408889634f};
+              decode_piece_cost(D, P), a.sm_scale * 1.4426950408889634f};
   e = launch_pdl(decode_kernel<D, P, Deep>, dim3(a.grid), dim3(kDecThreads), smem, stream, tk, tv, p);
   if (e != cudaSuccess) return e;
   MergeParams mp{a.partials, a.merge_table, a.out, a.lse, kv.num_q_heads, kv.num_kv_heads,
