@@ -29,10 +29,12 @@ struct NvtxRange {
 constexpr int kMaxSegments = 4096;     // batch * Hkv handled by one call
 constexpr int kMaxPages = 1 << 20;     // max_pages bound (int32 page-space arithmetic)
 // The decode splits its page sequence by weight: a list's first page weighs
-// 1 + decode_piece_cost(d, P) pages, the pages a CTA streams (~80 KiB of
-// K and V) in the time that ending a piece (its warps' merge) stalls it.
-constexpr int kDecodePieceBytes = 80 * 1024;
-constexpr int kMaxPieceCost = 32;
+// 1 + decode_piece_cost(d, P) pages, about the K and V a CTA streams in the
+// time that ending a piece stalls it (its 8 warp pipelines drift 2-4 us
+// apart over a piece and all wait for the last, then merge). The measured
+// step time is flat for weights of 160-384 KiB and worse at 48 or 512 KiB.
+constexpr int kDecodePieceBytes = 256 * 1024;
+constexpr int kMaxPieceCost = 128;
 inline int decode_piece_cost(int head_dim, int page_size) {
   const int page_bytes = 4 * page_size * head_dim;  // K and V, bf16
   const int c = (kDecodePieceBytes + page_bytes / 2) / page_bytes;

@@ -6,9 +6,10 @@
 // Plan (every CTA, on the device): load lens[B*Hkv] into shared memory and
 // take their inclusive prefix; the concatenated lists form one sequence of
 // `total` pages. Each (segment, CTA) piece ends in a CTA-wide merge of the
-// warps' states, which drains that CTA's copy pipeline for about as long as
-// streaming ~80 KiB takes, so the first page of every non-empty list weighs
-// 1 + piece_cost pages and the sequence is split evenly by weight over the G
+// warps' states: the warps, which drift apart over a piece, all wait for the
+// last one, so the CTA's copy pipeline idles for several microseconds. The
+// first page of every non-empty list therefore weighs 1 + piece_cost pages
+// (about 256 KiB of K and V) and the sequence is split evenly by weight over the G
 // CTAs: a CTA whose range starts more lists takes fewer pages, and the split
 // still depends on the list lengths alone. Each piece produces one partial
 // (m, l, o) in slot segment + CTA of the workspace, which is unique because
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   // Weighted split: page j of segment s weighs 1, plus X when j = prefix[s];
   // W(j) = weight of the pages before j. CTA c takes the pages whose W lies
   // in the c-th even share of the total weight (< 2^31: the host checks
-  // B * Hkv * (max_pages + 32)).
+  // B * Hkv * (max_pages + 128)).
   const int wtotal = wstart[S];
   const int geff = wtotal < G ? wtotal : G;
   const EvenSplit split(wtotal, geff > 0 ? geff : 1);

@@ -34,7 +34,7 @@
  * - Shapes supported: head_dim d in {64, 128}; page_size P in {16, 32, 64};
  *   num_kv_heads Hkv in {1, 2, 4, 8}; GQA group g = Hq / Hkv in {1, 2, 4, 8};
  *   batch * Hkv <= 4096 segments; max_pages <= 1<<20;
- *   batch * Hkv * (max_pages + 32) < 2^31 and num_phys_pages * Hkv * P < 2^31
+ *   batch * Hkv * (max_pages + 128) < 2^31 and num_phys_pages * Hkv * P < 2^31
  *   (int32 page-space and cache-row indices). Anything else returns
  *   ASP_EUNSUPPORTED.
  * - The current CUDA device when a call is made must be the device that owns
