@@ -247,7 +247,7 @@ asp_status asp_sparse_decode(const asp_paged_kv* kv, const float* q, const int32
   uint8_t* w = static_cast<uint8_t*>(ws);
   DecodeArgs a{kv, q, lists, lens, sm_scale, out, lse,
                reinterpret_cast<float*>(w + lay.partials_off),
-               reinterpret_cast<int32_t*>(w + lay.table_off), reinterpret_cast<uint32_t*>(w),
+               reinterpret_cast<int32_t*>(w + lay.arrivals_off), reinterpret_cast<uint32_t*>(w),
                lay.decode_grid, lay.slot_floats};
   return from_cuda(launch_decode(a, static_cast<cudaStream_t>(stream)));
 }

@@ -44,10 +44,12 @@ constexpr int kMaxGroup = 8;           // query heads per KV head (padded mma wi
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a bounded on-chip wait gives up after 2 s
 
 // ----------------------------------------------------------------- workspace
-// [ header 256 B | merge_table int32[S] | scores f32[S*max_pages] | partials ]
+// [ header 256 B | arrivals int32[S] | scores f32[S*max_pages] | partials ]
+// arrivals[s] counts the decode CTAs done with split segment s; the CTA that
+// completes it merges s and puts the count back to zero.
 // header word 0 is the sticky device error mask.
 struct WsLayout {
-  size_t table_off = 0;
+  size_t arrivals_off = 0;
   size_t scores_off = 0;
   size_t partials_off = 0;
   size_t total = 0;
@@ -62,8 +64,8 @@ inline WsLayout ws_layout(const asp_paged_kv& kv, int num_sms) {
   const size_t S = size_t(kv.batch) * kv.num_kv_heads;
   w.decode_grid = num_sms;
   w.slot_floats = 2 * kMaxGroup + kMaxGroup * kv.head_dim;
-  w.table_off = 256;
-  w.scores_off = align256(w.table_off + S * sizeof(int32_t));
+  w.arrivals_off = 256;
+  w.scores_off = align256(w.arrivals_off + S * sizeof(int32_t));
   w.partials_off = align256(w.scores_off + S * size_t(kv.max_pages) * sizeof(float));
   w.total = align256(w.partials_off +
                      (S + size_t(w.decode_grid)) * size_t(w.slot_floats) * sizeof(float));
@@ -360,7 +362,7 @@ struct DecodeArgs {
   float* out;
   float* lse;
   float* partials;
-  int32_t* merge_table;
+  int32_t* arrivals;  // [S], zero between calls
   uint32_t* err;
   int grid;
   int slot_floats;

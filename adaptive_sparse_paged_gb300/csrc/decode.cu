@@ -14,10 +14,12 @@
 // still depends on the list lengths alone. Each piece produces one partial
 // (m, l, o) in slot segment + CTA of the workspace, which is unique because
 // both indices grow along the sequence; a segment held whole by one CTA is
-// written out directly. A small second kernel merges the split segments by
-// log-sum-exp. The streaming kernel thus never fences, counts or waits on
-// another CTA: under full HBM load each such round trip costs 1.5-2 us, and
-// at a piece end it would stall that CTA's copy pipeline.
+// written out directly. A split segment is merged by log-sum-exp by the last
+// of its CTAs to finish: each counts its piece in with one atomic after its
+// stream has ended (never at a piece end, where the round trip, 1.5-2 us
+// under full HBM load, would stall the copy pipeline), and the CTA that
+// completes the count folds the pieces in CTA order, so the result does not
+// depend on timing. No CTA ever waits on another.
 //
 // Data path (per CTA: 8 warps, one CTA per SM): every warp runs its own
 // pipeline. Warp w takes stages w, w+8, ... of the CTA's slice (a stage is a
@@ -82,7 +84,7 @@ struct DecParams {
   float* out;
   float* lse;
   float* partials;
-  int32_t* merge_table;
+  int32_t* arrivals;  // [S]: pieces of each split segment done; zero between calls
   uint32_t* err;
   int B, Hq, Hkv, g, max_pages, num_phys, slot_floats;
   int piece_cost;  // extra weight of a list's first page in the split, in pages
@@ -117,6 +119,53 @@ __device__ __forceinline__ int seg_of(const int* prefix, int S, int pos) {
   return lo;
 }
 
+// Log-sum-exp merge of four output elements (query column col, channels
+// o_off .. o_off + 3 with o_off = col * d + channel) over the np partials
+// (m, l, o) of a segment, stored slot_floats apart from base: pieces are
+// folded in CTA order with an online rescale in the log2 domain, eight
+// pieces' loads in flight at once. The partials were written by other CTAs
+// of this grid: loads go through L2.
+__device__ __forceinline__ void fold_pieces4(const float* base, int np, int slot_floats, int col,
+                                             int o_off, float& M, float& L, float4& acc) {
+  M = -INFINITY;
+  L = 0.f;
+  acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  constexpr int kU = 8;
+  for (int c = 0; c < np; c += kU) {
+    float m[kU], l[kU];
+    float4 o[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      m[u] = -INFINITY;
+      if (c + u < np) {
+        const float* q = base + (size_t)(c + u) * slot_floats;
+        m[u] = __ldcg(q + col);
+        l[u] = __ldcg(q + 8 + col);
+        o[u] = __ldcg(reinterpret_cast<const float4*>(q + 16 + o_off));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (m[u] == -INFINITY) continue;  // a piece with no valid token (or none)
+      if (m[u] > M) {
+        const float sc = exp2f(M - m[u]);  // 0 while M is still -inf
+        acc.x *= sc;
+        acc.y *= sc;
+        acc.z *= sc;
+        acc.w *= sc;
+        L *= sc;
+        M = m[u];
+      }
+      const float w = exp2f(m[u] - M);
+      acc.x += w * o[u].x;
+      acc.y += w * o[u].y;
+      acc.z += w * o[u].z;
+      acc.w += w * o[u].w;
+      L += w * l[u];
+    }
+  }
+}
+
 template <int D, int P, bool Deep>
 __global__ void __launch_bounds__(kDecThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -129,7 +178,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   float* merge = reinterpret_cast<float*>(ring + C::kRingBytes);
   int4* meta = reinterpret_cast<int4*>(merge + C::kMergeFloats);         // [warp][slot]
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + kDecWarps * C::kSlots);
-  int* flags = reinterpret_cast<int*>(full + kDecWarps * C::kSlots);    // [0..2] merge, [8..] scan
+  int* flags = reinterpret_cast<int*>(full + kDecWarps * C::kSlots);    // [0..1] merge, [8..] scan
   int* prefix = flags + 48;                                              // [S + 1]
 
   // Split weight at the start of each segment, W(prefix[s]) = prefix[s] +
@@ -237,18 +286,19 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       p.out[((size_t)b * p.Hq + h * p.g + e / D) * D + e % D] = 0.f;
     for (int e = tid; e < p.g; e += kDecThreads) p.lse[(size_t)b * p.Hq + h * p.g + e] = -INFINITY;
   }
-  // Merge table for the merge kernel: entry s = (first CTA << 16) | last CTA
-  // holding a piece of segment s; equal halves mean nothing to merge.
-  if (cta == 0) {
-    for (int s = tid; s < S; s += kDecThreads) {
-      int t = 0;
-      if (prefix[s + 1] > prefix[s]) {
-        const int cf = split.part_of(wstart[s]);
-        const int cl = split.part_of(weight_at(s, prefix[s + 1] - 1));
-        t = (cf << 16) | cl;
-      }
-      p.merge_table[s] = t;
-    }
+  // Only a CTA's first and last pieces can hold part of a segment (a middle
+  // piece holds a whole one). For each, the CTAs cf..cf+np-1 holding that
+  // segment: the last of them to finish merges it.
+  int seg_a = -1, seg_b = -1, cf_a = 0, cf_b = 0, np_a = 0, np_b = 0;
+  if (beg < end) {
+    auto holders = [&](int s, int& cf) {
+      cf = split.part_of(wstart[s]);
+      return split.part_of(weight_at(s, prefix[s + 1] - 1)) - cf + 1;
+    };
+    seg_a = seg_of(prefix, S, (int)beg);
+    seg_b = seg_of(prefix, S, (int)(end - 1));
+    np_a = holders(seg_a, cf_a);
+    if (seg_b != seg_a) np_b = holders(seg_b, cf_b);
   }
   __syncthreads();  // the weights are done with: the ring is free for copies
   if (beg >= end) return;
@@ -536,67 +586,43 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   // never leave the CTA with copies in flight (only after a timeout can any remain)
   if (lane == 0)
     for (int n = waited; n < ni; ++n) mbar_wait(&my_full[n % C::kSlots], (n / C::kSlots) & 1);
-}
 
-// Merges the partials of every segment that the decode kernel split across
-// CTAs (one CTA per segment; segments held by one CTA exit at once). Pieces
-// are combined in CTA order, so the result does not depend on timing.
-struct MergeParams {
-  const float* partials;
-  const int32_t* merge_table;
-  float* out;
-  float* lse;
-  int Hq, Hkv, g, D, slot_floats;
-};
-
-// One CTA per split segment, one thread per output element (query head col,
-// channel d). After the merge-table entry every load is independent: a thread
-// reads each piece's (m, l) for its head (the same words across a warp, since
-// a warp never spans two heads) and its own element of each piece's output,
-// and folds them in with an online log-sum-exp in the log2 domain.
-__global__ void __launch_bounds__(1024) merge_kernel(const MergeParams p) {
-  const int s = blockIdx.x, tid = threadIdx.x, D = p.D;
-  pdl_launch_dependents();
-  pdl_wait_predecessor();
-  const int t = p.merge_table[s];
-  const int cf = t >> 16, cl = t & 0xffff;
-  if (cf >= cl || tid >= p.g * D) return;
-  const int col = tid / D, d = tid % D;
-  const float* base = p.partials + (size_t)(s + cf) * p.slot_floats;
-  const int np = cl - cf + 1;
-  float M = -INFINITY, L = 0.f, acc = 0.f;
-  auto fold = [&](float m, float l, float o) {
-    if (m == -INFINITY) return;  // a piece with no valid token
-    if (m > M) {
-      const float sc = exp2f(M - m);  // 0 while M is still -inf
-      acc *= sc;
-      L *= sc;
-      M = m;
-    }
-    const float w = exp2f(m - M);
-    acc += w * o;
-    L += w * l;
-  };
-  constexpr int kU = 8;  // pieces whose loads are in flight together
-  for (int c = 0; c < np; c += kU) {
-    float m[kU], l[kU], o[kU];
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      m[u] = -INFINITY;
-      if (c + u < np) {
-        const float* q = base + (size_t)(c + u) * p.slot_floats;
-        m[u] = q[col];
-        l[u] = q[8 + col];
-        o[u] = q[16 + col * D + d];
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kU; ++u) fold(m[u], l[u], o[u]);
+  // ---- split segments: count this CTA's pieces in; the CTA that brings a
+  // segment's count to its number of pieces merges that segment's partials
+  // (in CTA order, so the result does not depend on which CTA it is) and
+  // resets the count for the next call.
+  if (np_a < 2 && np_b < 2) return;  // CTA-uniform
+  __syncthreads();  // every partial store of this CTA has been issued
+  if (tid == 0) {
+    __threadfence();  // ... and is ordered before the arrivals (cumulative over the CTA)
+    const int oa = np_a > 1 ? atomicAdd(&p.arrivals[seg_a], 1) : -1;
+    const int ob = np_b > 1 ? atomicAdd(&p.arrivals[seg_b], 1) : -1;
+    flags[0] = np_a > 1 && oa == np_a - 1 ? 1 : 0;
+    flags[1] = np_b > 1 && ob == np_b - 1 ? 1 : 0;
+    __threadfence();  // the other CTAs' partials, seen through the arrivals, before the loads
   }
-  const int b = s / p.Hkv, h = s % p.Hkv;
-  const size_t row = (size_t)b * p.Hq + h * p.g + col;
-  p.out[row * D + d] = L > 0.f ? acc / L : 0.f;
-  if (d == 0) p.lse[row] = L > 0.f ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
+  __syncthreads();
+#pragma unroll 1
+  for (int k = 0; k < 2; ++k) {
+    if (!flags[k]) continue;  // CTA-uniform
+    const int ms = k ? seg_b : seg_a, cf = k ? cf_b : cf_a, np = k ? np_b : np_a;
+    const float* base = p.partials + (size_t)(ms + cf) * p.slot_floats;
+    const int mb = ms / p.Hkv, mh = ms % p.Hkv;
+    for (int e = 4 * tid; e < p.g * D; e += 4 * kDecThreads) {  // one pass when g * d <= 1024
+      const int col = e / D, d = e % D;
+      float M, L;
+      float4 acc;
+      fold_pieces4(base, np, p.slot_floats, col, e, M, L, acc);
+      const size_t row = (size_t)mb * p.Hq + mh * p.g + col;
+      float* o = p.out + row * D + d;  // the caller's buffer: 4-byte alignment only
+      o[0] = L > 0.f ? acc.x / L : 0.f;
+      o[1] = L > 0.f ? acc.y / L : 0.f;
+      o[2] = L > 0.f ? acc.z / L : 0.f;
+      o[3] = L > 0.f ? acc.w / L : 0.f;
+      if (d == 0) p.lse[row] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+    }
+    if (tid == 0) p.arrivals[ms] = 0;
+  }
 }
 
 // ----------------------------------------------------------------- host side
@@ -668,16 +694,11 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
   if ((e = make_page_map(&tk, kv.k_cache, rows, D, P)) != cudaSuccess) return e;
   if ((e = make_page_map(&tv, kv.v_cache, rows, D, P)) != cudaSuccess) return e;
   DecParams p{a.q, a.lists, a.lens, kv.block_table, kv.seq_lens, a.out, a.lse, a.partials,
-              a.merge_table, a.err, kv.batch, kv.num_q_heads, kv.num_kv_heads,
+              a.arrivals, a.err, kv.batch, kv.num_q_heads, kv.num_kv_heads,
               kv.num_q_heads / kv.num_kv_heads, kv.max_pages, kv.num_phys_pages, a.slot_floats,
               decode_piece_cost(D, P), a.sm_scale * 1.4426950408889634f};
-  e = launch_pdl(decode_kernel<D, P, Deep>, dim3(a.grid), dim3(kDecThreads), smem, stream, tk, tv, p);
-  if (e != cudaSuccess) return e;
-  MergeParams mp{a.partials, a.merge_table, a.out, a.lse, kv.num_q_heads, kv.num_kv_heads,
-                 kv.num_q_heads / kv.num_kv_heads, D, a.slot_floats};
-  if ((e = set_max_dynamic_smem((const void*)merge_kernel, 0)) != cudaSuccess) return e;
-  return launch_pdl(merge_kernel, dim3(S), dim3((kv.num_q_heads / kv.num_kv_heads) * D), 0, stream,
-                    mp);
+  return launch_pdl(decode_kernel<D, P, Deep>, dim3(a.grid), dim3(kDecThreads), smem, stream, tk, tv,
+                    p);
 }
 
 // The deeper ring when its shared memory (which grows with the segment

@@ -1,6 +1,6 @@
 """One decode step over L layers, optionally captured into a single CUDA graph.
 
-Per layer: asp_coverage_select (score + select kernels) then asp_sparse_decode
+Per layer: asp_coverage_select (one cluster kernel, or score + select kernels) then asp_sparse_decode
 (self-planning attention), and optionally asp_page_summarize in APPEND mode
 first. The layers share one workspace; stream order serialises them. Nothing
 returns to the host between layers, which is what lets the whole step live
@@ -56,11 +56,11 @@ class DecodeStep:
 
     # kernel launches of one step, per layer: the selection's (one cluster
     # kernel, or a score pass and a select kernel; select alone at gamma = 1),
-    # decode + merge, and the append kernel when enabled
+    # the decode, and the append kernel when enabled
     @property
     def launches_per_step(self) -> int:
         per, _ = B.asp_select_plan(self.kvs[0], self.gamma, self.budget)
-        return len(self.kvs) * (per + 2 + (1 if self.append is not None else 0))
+        return len(self.kvs) * (per + 1 + (1 if self.append is not None else 0))
 
     def run_layer(self, l: int, stream=None, events=None):
         kv = self.kvs[l]
@@ -152,10 +152,10 @@ class DecodeLoop:
 
     @property
     def launches(self) -> int:
-        """Kernel launches of the whole loop: [append,] the selection's, decode, merge."""
+        """Kernel launches of the whole loop: [append,] the selection's, the decode."""
         per, _ = B.asp_select_plan(self.kvs[0][0], self.gamma, self.budget,
                                    append=self.fused_append)
-        return self.n * self.L * ((0 if self.fused_append else 1) + per + 2)
+        return self.n * self.L * ((0 if self.fused_append else 1) + per + 1)
 
     def run(self, stream=None):
         for i in range(self.n):

@@ -122,11 +122,12 @@ const char* asp_status_string(asp_status status);
  * asp_page_summarize for this shape on the CURRENT device (the decode grid
  * is sized from its SM count). Writes the size to *bytes. The workspace is a
  * caller-owned device buffer, 256-byte aligned, that must be zeroed once with
- * asp_workspace_init before first use. It holds the device error word and
- * per-call scratch (page scores, the decode's partial results and merge
- * table) that every call rewrites before reading, so no call depends on what
- * an earlier one left and graph replay is safe. Calls that share one
- * workspace must be ordered on one stream.
+ * asp_workspace_init before first use. It holds the device error word,
+ * per-call scratch (page scores, the decode's partial results) that every
+ * call rewrites before reading, and one arrival count per segment that the
+ * decode leaves at zero when it ends, so graph replay is safe. Calls that
+ * share one workspace must be ordered on one stream; after a device error
+ * (asp_get_device_error non-zero) zero it again with asp_workspace_init.
  */
 asp_status asp_workspace_size(const asp_paged_kv* kv, size_t* bytes);
 
@@ -236,12 +237,13 @@ asp_status asp_page_scores(const asp_paged_kv* kv, const float* q, float* scores
  * valid tokens of the listed pages:
  *   out[b,h,:] = sum_t softmax_t(sm_scale * q[b,h].k_t) v_t
  *   lse[b,h]   = log sum_t exp(sm_scale * q[b,h].k_t)
- * The grid is a fixed number of CTAs (one per SM); each loads the lengths,
- * splits the concatenated lists evenly and attends over its slice. A CTA
- * whose slice holds a whole segment writes out/lse itself; otherwise it
- * leaves a partial (max, sum, unnormalised output) in the workspace, and a
- * second kernel, enqueued by the same call, combines a segment's partials by
- * log-sum-exp. A segment with lens 0 gets out = 0, lse = -inf.
+ * One kernel launch: a fixed number of CTAs (one per SM); each loads the
+ * lengths, splits the concatenated lists by weight (a list's first page
+ * weighs more than the others) and attends over its slice. A CTA whose slice
+ * holds a whole segment writes out/lse itself; otherwise it leaves a partial
+ * (max, sum, unnormalised output) in the workspace, and the last CTA of the
+ * segment to finish combines its partials by log-sum-exp, in CTA order. A
+ * segment with lens 0 gets out = 0, lse = -inf.
  * K/V are bf16; the products run on tensor cores with fp32 accumulation and
  * the probabilities are rounded to bf16 for the P.V product.
  * lists, lens : as written by asp_coverage_select (any order within a list).

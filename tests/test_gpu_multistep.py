@@ -117,5 +117,5 @@ def test_decode_loop_replay_is_stable(cuda_device):
     torch.cuda.synchronize()
     assert B.asp_get_device_error(loop.ws) == 0
     assert torch.equal(case.kvs[0].k_cache, k1)
-    assert loop.launches == n * 1 * 4  # fused append: score, select, decode, merge
+    assert loop.launches == n * 1 * 3  # fused append: score, select, decode
     assert [int(x[0]) for x in loop.seq_lens] == [T0[0] + i + 1 for i in range(n)]
