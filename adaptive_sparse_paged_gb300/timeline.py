@@ -28,7 +28,7 @@ PKG = "adaptive_sparse_paged_gb300"
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 
-SEL_SLOTS = ("start", "waited", "streamed", "barrier 1", "barrier 2", "barrier 3", "end")
+SEL_SLOTS = ("start", "waited", "streamed", "barrier 1", "barrier 2", "barrier 3", "end", "cutoff", "candidates")
 DEC_SLOTS = ("start", "waited", "planned", "first data", "streamed", "arrived", "merged", "smid")
 N_LAUNCH, N_CTA = 64, 160  # launches kept (ring) and CTAs per launch recorded
 
@@ -79,6 +79,9 @@ def patches():
          + _stamp("sel", ns, 4) + "\n"),
         ("  cluster.sync();  // barrier 3: every CTA holds every candidate\n",
          "  cluster.sync();  // barrier 3: every CTA holds every candidate\n  " + _stamp("sel", ns, 5) + "\n"),
+        ("  // ------------------------------------- 7. kept ids, ascending, per CTA\n",
+         "  " + _stamp("sel", ns, 7) + "\n  " + _stamp("sel", ns, 8, value="1ull + nc")
+         + "\n  // ------------------------------------- 7. kept ids, ascending, per CTA\n"),
         ("      }\n    }\n  }\n}\n\n// Pieces per warp fetched",
          "      }\n    }\n  }\n  __syncthreads();\n  " + _stamp("sel", ns, 6) + "\n}\n\n// Pieces per warp fetched"),
     ]
@@ -133,19 +136,27 @@ def _median_rows(sel, dec, layers):
         x = a[:, i]
         return x[x > 0].astype(np.float64)
 
-    rows = {}
-    def add(k, v):
+    rows, counts = {}, {}
+
+    def add(k, v):  # a time in ns
         rows.setdefault(k, []).append(v)
+
+    def add_count(k, v):  # a count or a fraction
+        counts.setdefault(k, []).append(v)
     for l in range(min(4, layers // 4), layers - min(4, layers // 4) - 1):
         s, d, s_next = sel[l], dec[l], sel[l + 1]
         if not len(col(s, 0)):
             continue
         t0 = col(s, 0).min()
         w = np.median(col(s, 1))
-        for i, name in enumerate(SEL_SLOTS):
+        for i, name in enumerate(SEL_SLOTS[:8]):
             c = col(s, i)
             if len(c):
                 add(f"select {name} (median CTA)", np.median(c) - t0)
+        c = col(s, 8)
+        if len(c):
+            add_count("select CTAs with > 32 candidates (fraction)", float(np.mean(c - 1 > 32)))
+            add_count("select candidates per cluster (median)", float(np.median(c - 1)))
         if len(col(s, 6)):
             add("select end (last CTA)", col(s, 6).max() - t0)
         for i, name in enumerate(DEC_SLOTS[:5]):
@@ -159,7 +170,9 @@ def _median_rows(sel, dec, layers):
         if len(col(s_next, 1)):
             add("next select waited (median CTA)", np.median(col(s_next, 1)) - t0)
             add("layer period (select waited to next)", np.median(col(s_next, 1)) - w)
-    return {k: float(np.median(v)) / 1e3 for k, v in rows.items()}
+    out = {k: float(np.median(v)) / 1e3 for k, v in rows.items()}
+    out.update({k: float(np.median(v)) for k, v in counts.items()})
+    return out
 
 
 def _sm_consistency(dec, layers):
