@@ -784,14 +784,17 @@ __global__ void __launch_bounds__(kCsThreads, 1)
   }
 }
 
-// Pieces per warp fetched into L2 before the previous kernel ends.
-constexpr int kCsPrefetchPieces = 3;
-// Kept pages per CTA whose K/V the kernel fetches into L2 for the decode
-// (8 KiB each at P = 16, d = 128). At 128k, gamma = 0.99 on one GB300 (one
-// box, two repeats each): 0 pages 365.5 steps/s, 32 372.6, 64 369.1, 128
-// 364.9, 256 339.4. More pages make this kernel slower than they make the
-// decode faster.
-constexpr int kCsKvPrefetchPages = 32;
+// Pieces per warp fetched into L2 before the previous kernel ends, and kept
+// pages per CTA whose K/V the kernel fetches into L2 for the decode (8 KiB
+// each at P = 16, d = 128). Outstanding bulk prefetches hold this kernel
+// open, so more pages make it slower than they make the decode faster. At
+// 128k, gamma = 0.99 on one GB300 (builds alternated on one box, steps/s):
+// (pages, pieces) = (0, 3) 365.5, (32, 3) 372.6, (64, 3) 369.1, (128, 3)
+// 364.9, (256, 3) 339.4; on a later build of the decode, (32, 3) 390.7,
+// (24, 6) 393.6, (28, 6) 393.6, (24, 8) 393.6, and on another box (16, 3)
+// 391.9, (48, 3) 391.9, (32, 4) 394.8, (24, 4) 395.3 against (32, 3) 393.7.
+constexpr int kCsPrefetchPieces = 6;
+constexpr int kCsKvPrefetchPages = 24;
 
 template <int D, int G, int C, bool Append>
 cudaError_t launch_cs(const SelectArgs& a, cudaStream_t stream) {
