@@ -203,12 +203,20 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const int per = ceil_div(S, kDecThreads);
   const int a0 = min(S, tid * per), a1 = min(S, a0 + per);
   int run = 0, nzr = 0;
+  // Range errors are collected and reported once after the loop: an atomic
+  // on the error word between loads would keep the later loads in order.
+  uint32_t bad = 0;
+  const long long t_cap = (long long)p.max_pages * P;
   for (int s = a0; s < a1; ++s) {  // wstart[s + 1] first holds non-empty segments up to s
-    const int b = s / p.Hkv;
-    const int n_b = ceil_div(clamp_seq_len(p.seq_lens[b], p.max_pages, P, p.err), P);
+    int Tb = p.seq_lens[s / p.Hkv];
     int n = p.lens[s];
+    if (Tb < 0 || (long long)Tb > t_cap) {
+      bad |= ASP_DEVERR_SEQ_RANGE;
+      Tb = Tb < 0 ? 0 : (int)t_cap;
+    }
+    const int n_b = ceil_div(Tb, P);
     if (n < 0 || n > n_b) {
-      report(p.err, ASP_DEVERR_LEN_RANGE);
+      bad |= ASP_DEVERR_LEN_RANGE;
       n = n < 0 ? 0 : n_b;
     }
     run += n;
@@ -216,6 +224,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     prefix[s + 1] = run;
     wstart[s + 1] = nzr;
   }
+  if (bad) report(p.err, bad);
   int x = run, y = nzr;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
