@@ -29,7 +29,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 
 SEL_SLOTS = ("start", "waited", "streamed", "barrier 1", "barrier 2", "barrier 3", "end", "cutoff", "candidates")
-DEC_SLOTS = ("start", "waited", "planned", "first data", "streamed", "arrived", "merged", "smid")
+DEC_SLOTS = ("start", "waited", "planned", "first data", "streamed", "arrived", "merged", "smid",
+             "lengths loaded", "prefix done")
 N_LAUNCH, N_CTA = 64, 160  # launches kept (ring) and CTAs per launch recorded
 
 
@@ -100,6 +101,9 @@ def patches():
         ("        if (__all_sync(kFull, got)) {\n          waited = nc + 1;",
          "        if (__all_sync(kFull, got)) {\n          if (nc == 0) { "
          + _stamp("dec", nd, 3, "warp == 0 && lane == 0") + " }\n          waited = nc + 1;"),
+        ("  if (bad) report(p.err, bad);\n", "  if (bad) report(p.err, bad);\n  " + _stamp("dec", nd, 8) + "\n"),
+        ("  // Weighted split: page j of segment s weighs 1, plus X when j = prefix[s];\n",
+         "  " + _stamp("dec", nd, 9) + "\n  // Weighted split: page j of segment s weighs 1, plus X when j = prefix[s];\n"),
         ("  // never leave the CTA with copies in flight",
          "  " + _stamp("dec", nd, 4) + "\n  " + smid + "\n  // never leave the CTA with copies in flight"),
         ("    flags[1] = np_b > 1 && ob == np_b - 1 ? 1 : 0;\n",
@@ -159,10 +163,10 @@ def _median_rows(sel, dec, layers):
             add_count("select candidates per cluster (median)", float(np.median(c - 1)))
         if len(col(s, 6)):
             add("select end (last CTA)", col(s, 6).max() - t0)
-        for i, name in enumerate(DEC_SLOTS[:5]):
+        for i in (0, 1, 8, 9, 2, 3, 4):
             c = col(d, i)
             if len(c):
-                add(f"decode {name} (median CTA)", np.median(c) - t0)
+                add(f"decode {DEC_SLOTS[i]} (median CTA)", np.median(c) - t0)
         if len(col(d, 4)):
             add("decode streamed (last CTA)", col(d, 4).max() - t0)
         if len(col(d, 6)):
