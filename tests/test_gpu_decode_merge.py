@@ -72,20 +72,22 @@ def test_one_segment_held_by_every_cta(cuda_device):
     assert not _arrivals(case).any()
 
 
-@pytest.mark.parametrize("gamma", [0.9, 0.99])
-def test_many_short_segments_of_mixed_lengths(cuda_device, gamma):
+@pytest.mark.parametrize("d,gamma", [(64, 0.9), (64, 0.99), (128, 0.99)])
+def test_many_short_segments_of_mixed_lengths(cuda_device, d, gamma):
     """256 segments of 1 to 700 pages: CTAs hold several pieces and complete
     up to two segments each; lists and outputs against the oracle, counts
-    back to zero, a repeat bit-identical."""
+    back to zero, a repeat bit-identical. At d = 128 the prefix of 256
+    segment lengths no longer fits beside the deep ring, so the decode runs
+    its shallower ring."""
     rng = np.random.default_rng(72)
     seq_lens = [int(x) for x in rng.integers(1, 16 * 700, size=64)]
     seq_lens[3] = 0
     seq_lens[7] = 16
-    w = small("mixed_short", 64, 8, 4, 64, 16, max(seq_lens))
+    w = small(f"mixed_short_d{d}", 64, 8, 4, d, 16, max(seq_lens))
     case = Case(w, seed=73, device=cuda_device, seq_lens=seq_lens)
     lists, lens, out, lse = case.run(0, gamma)
     assert not _arrivals(case).any(), "arrival count left non-zero"
-    check_case(case, 0, gamma, 0, lists, lens, out, lse, what=f"mixed_short gamma {gamma}")
+    check_case(case, 0, gamma, 0, lists, lens, out, lse, what=f"mixed_short d{d} gamma {gamma}")
     out2, lse2 = _decode(case, lists, lens)
     assert torch.equal(out, out2) and torch.equal(lse, lse2), "repeat differs"
     assert not _arrivals(case).any()
