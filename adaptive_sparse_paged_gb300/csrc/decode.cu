@@ -250,8 +250,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   off += x - run;
   offn += y - nzr;
   // Every share of the weight must hold a page (X + 1 <= share size), so that
-  // the CTAs holding pieces of one segment are consecutive, as the merge
-  // kernel assumes: X is capped at total / G - 1.
+  // the CTAs holding pieces of one segment are consecutive, as the merge at
+  // the end assumes (it folds the partial slots of CTAs cf..cl): X is capped
+  // at total / G - 1.
   const int X = max(0, min(p.piece_cost, total / G - 1));
   for (int s = a0; s < a1; ++s) {
     prefix[s + 1] += off;
